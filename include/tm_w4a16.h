@@ -1,0 +1,117 @@
+/*
+ * tm_w4a16.h -- C ABI of the GB300 (sm_103a) W4A16 mixed-precision GEMM.
+ *
+ *   Y[M,N] = X[M,K] . dequant(W),   dequant(w)[k][n] = (q[k][n] - z[k/g][n]) * s[k/g][n]
+ *
+ * W is stored as unsigned 4-bit codes q (0..15), grouped along K in groups of
+ * g weights, with one fp16 scale s and one 4-bit zero z per (group, column).
+ * X and Y are fp16; products accumulate in fp32.
+ *
+ * Sources: the dequantisation rule is that of "LMDeploy Guide: Fast
+ * Mixed-Precision LLM Inference Engine", section 3 ("Instruction-Level
+ * Parallelism (ILP) for Zero-Overhead Dequantization"); groups run along K
+ * with one scale per group ("LMDeploy, in depth", section "Quantization: AWQ
+ * weights and KV cache"); the weights are repacked once, offline, into the
+ * order the kernels consume so that no layout change happens at run time (the
+ * guide, section 1 "Hardware-Aware Weight Packing").
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" must point to memory of the current CUDA device.
+ *   - fp16 values travel as their 16-bit patterns (uint16_t) or as void*.
+ *   - Nothing throws; every call returns a tm_status (or nothing).
+ *   - Shapes: g in {64, 128}; K > 0 and K % g == 0; N > 0 and N % 16 == 0;
+ *     M >= 0 (M == 0 is a no-op).
+ */
+#ifndef TM_W4A16_H
+#define TM_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TM_OK = 0,
+  TM_ERR_INVALID_ARG = 1,   /* null pointer, bad shape or group size */
+  TM_ERR_ALIGNMENT = 2,     /* a pointer is not 16-byte aligned */
+  TM_ERR_UNSUPPORTED = 3,   /* valid request this build does not serve (e.g. no sm_103a device) */
+  TM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  TM_ERR_DEVICE_TIMEOUT = 5,/* a kernel gave up waiting on a barrier (reported by tm_device_error) */
+  TM_ERR_BAD_CODE = 6       /* a code or zero above 15 was passed to tm_pack_weights */
+} tm_status;
+
+/* Opaque packed weights.  Owns one device allocation (codes, scales, zeros in
+ * the kernels' order) on the device that was current at tm_pack_weights. */
+typedef struct tm_packed tm_packed;
+
+/* Optional launch settings for tm_w4a16_gemm_ex; zero fields mean "automatic". */
+typedef struct {
+  int path;    /* 0 auto, 1 decode kernel (mma.sync, M <= 64), 2 prefill kernel (tcgen05) */
+  int split_k; /* 0 auto, else number of CTAs (a thread-block cluster, 1..8) sharing one output tile along K */
+  int tile_n;  /* 0 auto, else output columns per CTA (decode 64/128/256, prefill 128/256) */
+  int stages;  /* 0 auto, else pipeline depth in shared memory (2..8) */
+} tm_gemm_config;
+
+/* Human-readable name of a status (static string, never NULL). */
+const char* tm_status_str(tm_status s);
+
+/* Bytes of device memory tm_pack_weights allocates for a K x N layer with
+ * group size g.  Writes *bytes; TM_ERR_INVALID_ARG on a bad shape. */
+tm_status tm_packed_bytes(int K, int N, int g, size_t* bytes);
+
+/*
+ * Offline repack (the guide's section 1): reads the plain codes and scales
+ * and writes them, once, in the fragment order the GEMM kernels load.
+ *   q : device, uint8 [K][N] row-major, one code (0..15) per byte
+ *   z : device, uint8 [K/g][N], one zero (0..15) per byte
+ *   s : device, fp16 bits [K/g][N]
+ *   out: receives a new handle; the caller frees it with tm_packed_free.
+ * Synchronous: returns after the packing kernels finished on the current
+ * device.  TM_ERR_BAD_CODE if any q or z is above 15 (no handle is returned).
+ */
+tm_status tm_pack_weights(const uint8_t* q, const uint8_t* z, const uint16_t* s, int K, int N, int g,
+                          tm_packed** out);
+
+/* Inverse of tm_pack_weights (device pointers with the same layouts as its
+ * inputs; the caller owns them).  Synchronous.  pack -> unpack is bit-exact. */
+tm_status tm_unpack_weights(const tm_packed* p, uint8_t* q, uint8_t* z, uint16_t* s);
+
+/* K, N, g and the size of the device allocation of a handle (any out pointer may be NULL). */
+tm_status tm_packed_info(const tm_packed* p, int* K, int* N, int* g, size_t* bytes);
+
+/* Release a handle and its device memory (NULL is ignored). */
+void tm_packed_free(tm_packed* p);
+
+/*
+ * The product.  X: device fp16 [M][K] row-major, 16-byte aligned.
+ * Y: device fp16 [M][N] row-major, 16-byte aligned, written in full.
+ * stream: a cudaStream_t (NULL = the legacy default stream).
+ * Asynchronous on `stream`; no host synchronisation, no allocation.
+ * M <= 64 runs the decode kernel (split-K mma.sync GEMV/skinny GEMM),
+ * larger M the tcgen05 prefill kernel.  Different calls may share a handle
+ * concurrently: a call keeps no state outside its own launch.
+ */
+tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void* stream);
+
+/* tm_w4a16_gemm with explicit launch settings (cfg may be NULL = automatic). */
+tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config* cfg,
+                           void* stream);
+
+/* The settings tm_w4a16_gemm would use for this handle and M (all fields filled in). */
+tm_status tm_gemm_plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out);
+
+/* Sticky device-side error bits of the current device, set by kernels that
+ * gave up waiting (bit 0: barrier timeout).  Synchronises the device.
+ * clear != 0 resets them.  Returns TM_ERR_DEVICE_TIMEOUT when bit 0 was set. */
+tm_status tm_device_error(int clear, uint32_t* bits);
+
+/* Number of kernel launches the last tm_w4a16_gemm* call on this thread made (1 or 0). */
+int tm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TM_W4A16_H */

@@ -1,0 +1,90 @@
+"""The C ABI: the library builds, loads without a GPU and exports every entry
+point that include/tm_w4a16.h declares; host-side argument checks.  No
+compute call is made here."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADERS = glob.glob(os.path.join(ROOT, "include", "*.h"))
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(tm_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_quantized_gemm_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("tm_pack_weights", "tm_unpack_weights", "tm_w4a16_gemm", "tm_packed_bytes", "tm_packed_free",
+              "tm_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from w4a16_quantized_gemm_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (tm_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_binding_names_match_header():
+    from w4a16_quantized_gemm_gb300 import binding
+    assert sorted(binding.EXPORTS) == declared_functions()
+
+
+def test_status_strings(lib):
+    from w4a16_quantized_gemm_gb300 import binding
+    for st in range(7):
+        assert binding.status_str(st) == binding._STATUS[st]
+    assert binding.status_str(99) == "unknown status"
+
+
+@pytest.mark.parametrize("K,N,g,ok", [(4096, 4096, 128, True), (128, 16, 128, True), (192, 32, 64, True),
+                                      (4096, 4096, 32, False), (100, 4096, 64, False), (4096, 40, 128, False),
+                                      (0, 16, 64, False), (128, 0, 64, False)])
+def test_packed_bytes_validation(lib, K, N, g, ok):
+    out = ctypes.c_size_t()
+    st = lib.tm_packed_bytes(K, N, g, ctypes.byref(out))
+    assert (st == 0) == ok
+    if ok:
+        # codes + one fp16 scale and one 4-bit zero per (group, column), K padded to 2g
+        Kp = -(-K // (2 * g)) * (2 * g)
+        assert out.value >= Kp * N // 2 + (Kp // g) * N * 5 // 2
+
+
+def test_null_arguments_are_rejected(lib):
+    h = ctypes.c_void_p()
+    assert lib.tm_pack_weights(None, None, None, 128, 16, 64, ctypes.byref(h)) == 1
+    assert lib.tm_pack_weights(None, None, None, 128, 16, 64, None) == 1
+    assert lib.tm_unpack_weights(None, None, None, None) == 1
+    assert lib.tm_w4a16_gemm(None, None, None, 1, None) == 1
+    assert lib.tm_packed_info(None, None, None, None, None) == 1
+    lib.tm_packed_free(None)
+    assert lib.tm_last_launch_count() == 0
+
+
+def test_library_has_sm103a_code():
+    """The build targets sm_103a only (checked from the build flags)."""
+    from w4a16_quantized_gemm_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path against the fp64 oracle, through the C ABI.
+
+Bar: pack -> unpack bit-exact; GEMM max|Y - Y_ref| / max|Y_ref| <= 2e-3 on
+every compared element (all rows for M <= 256, a seeded subset plus the first
+and last rows above; rows of Y are independent, so a subset is an exact
+check of those rows)."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_util import TOL, activations, host_weights, packed, run_and_compare, sample_rows
+from w4a16_quantized_gemm_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+
+def _dev_u8(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _dev_f16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint16)).cuda().view(torch.float16)
+
+
+# ---------------------------------------------------------------- packing ----
+
+@pytest.mark.parametrize("K,N,g", [(4096, 4096, 128), (128, 16, 128), (192, 48, 64), (14336, 4096, 128),
+                                   (4096, 28672, 64), (384, 144, 128)])
+def test_pack_unpack_roundtrip_bit_exact(K, N, g):
+    q, z, s, _ = synth.weights(K, N, g)
+    w = binding.pack(_dev_u8(q), _dev_u8(z), _dev_f16(s), g)
+    q2, z2, s2 = w.unpack()
+    assert np.array_equal(q2.cpu().numpy(), q)
+    assert np.array_equal(z2.cpu().numpy(), z)
+    assert np.array_equal(s2.cpu().numpy().view(np.uint16), s.view(np.uint16))
+    assert w.nbytes == binding.packed_bytes(K, N, g)
+    w.free()
+
+
+def test_pack_rejects_bad_codes():
+    q, z, s, _ = synth.weights(256, 32, 128)
+    q = q.copy()
+    q[100, 7] = 16
+    with pytest.raises(binding.TMError) as e:
+        binding.pack(_dev_u8(q), _dev_u8(z), _dev_f16(s), 128)
+    assert e.value.status == 6
+    z = z.copy()
+    q[100, 7] = 3
+    z[1, 31] = 200
+    with pytest.raises(binding.TMError) as e:
+        binding.pack(_dev_u8(q), _dev_u8(z), _dev_f16(s), 128)
+    assert e.value.status == 6
+    assert binding.device_error() == 0
+
+
+# ------------------------------------------------------------ workloads -------
+
+def _cases(idx):
+    return [pytest.param(c, id=c.name) for c in synth.workload(idx)]
+
+
+@pytest.mark.parametrize("case", _cases(0) + _cases(1))
+def test_decode_workloads(case):
+    err, _ = run_and_compare(case.M, case.K, case.N, case.g, case.stress)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("case", _cases(2))
+def test_prefill_workloads(case):
+    err, _ = run_and_compare(case.M, case.K, case.N, case.g, case.stress)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("case", _cases(3))
+def test_llama70b_workloads(case):
+    err, _ = run_and_compare(case.M, case.K, case.N, case.g, case.stress)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("case", _cases(4))
+def test_stress_workloads(case):
+    err, _ = run_and_compare(case.M, case.K, case.N, case.g, case.stress)
+    assert err <= TOL, err
+
+
+# ------------------------------------------------------------ edge cases ------
+
+@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 15, 16, 17, 31, 32, 33, 48, 63, 64])
+def test_decode_ragged_m(M):
+    err, _ = run_and_compare(M, 1024, 384, 128, config={"path": 1})
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("M", [1, 33, 64, 65, 127, 128, 129, 200, 257])
+def test_prefill_ragged_m(M):
+    err, _ = run_and_compare(M, 1024, 384, 128, config={"path": 2})
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("K,N,g", [(128, 16, 128), (64, 16, 64), (192, 48, 64), (640, 272, 128), (896, 4112, 64)])
+def test_small_and_ragged_shapes(path, K, N, g):
+    """K = g (one group, odd group count), N one n-tile, N not a multiple of the CTA tile."""
+    err, _ = run_and_compare(5 if path == 1 else 130, K, N, g, config={"path": path})
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+def test_decode_split_and_tile_overrides(split, tile_n):
+    M = 8
+    err, _ = run_and_compare(M, 2048, 512, 128, config={"path": 1, "split_k": split, "tile_n": tile_n})
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("stages", [2, 3, 5])
+def test_decode_stage_override(stages):
+    err, _ = run_and_compare(16, 4096, 1024, 64, config={"path": 1, "stages": stages, "split_k": 2})
+    assert err <= TOL, err
+
+
+def test_m64_both_paths_agree_with_oracle():
+    e1, Y1 = run_and_compare(64, 4096, 1024, 128, config={"path": 1})
+    e2, Y2 = run_and_compare(64, 4096, 1024, 128, config={"path": 2})
+    assert e1 <= TOL and e2 <= TOL
+
+
+def test_m_zero_is_noop():
+    w = packed(1024, 384, 128)
+    X = torch.empty((0, 1024), dtype=torch.float16, device="cuda")
+    Y = binding.gemm(X, w)
+    assert Y.shape == (0, 384)
+    assert binding.last_launch_count() == 0
+
+
+def test_deterministic_bits():
+    for cfg in ({"path": 1, "split_k": 4}, {"path": 2}):
+        M = 16 if cfg["path"] == 1 else 256
+        w = packed(4096, 1024, 128)
+        X = torch.from_numpy(activations(M, 4096, 1024, 128).view(np.uint16)).cuda().view(torch.float16)
+        Y1 = binding.gemm(X, w, config=cfg).clone()
+        Y2 = binding.gemm(X, w, config=cfg).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(Y1.view(torch.int16), Y2.view(torch.int16))
+
+
+def test_unaligned_pointer_rejected():
+    w = packed(1024, 384, 128)
+    buf = torch.zeros(2 * 1024 + 8, dtype=torch.float16, device="cuda")
+    X = buf[1:1 + 1024].view(1, 1024)  # 2-byte offset
+    with pytest.raises(binding.TMError) as e:
+        binding.gemm(X, w)
+    assert e.value.status == 2
+
+
+def test_host_buffers_end_to_end():
+    """The same call with CPU (pinned) X: copies in, product, copy out."""
+    M, K, N, g = 8, 4096, 1024, 128
+    X = activations(M, K, N, g)
+    Xh = torch.from_numpy(X.view(np.uint16)).view(torch.float16).pin_memory()
+    Yh = binding.gemm(Xh, packed(K, N, g))
+    assert not Yh.is_cuda
+    q, z, s, _ = host_weights(K, N, g)
+    import oracle
+    err = oracle.rel_max_err(Yh.float().numpy().astype(np.float64), oracle.gemm(X, q, z, s, g))
+    assert err <= TOL
+
+
+def test_one_launch_per_call():
+    w = packed(1024, 384, 128)
+    X = torch.zeros((4, 1024), dtype=torch.float16, device="cuda")
+    binding.gemm(X, w)
+    assert binding.last_launch_count() == 1
+    X = torch.zeros((300, 1024), dtype=torch.float16, device="cuda")
+    binding.gemm(X, w)
+    assert binding.last_launch_count() == 1
+    torch.cuda.synchronize()
+
+
+def test_no_device_errors_left():
+    torch.cuda.synchronize()
+    assert binding.device_error(clear=False) == 0

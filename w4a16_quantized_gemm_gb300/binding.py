@@ -1,0 +1,229 @@
+"""Thin ctypes binding of ``include/tm_w4a16.h`` (argument marshalling only).
+
+Every step of the computation runs in the CUDA library; PyTorch provides
+device memory and streams.  If the library is missing this module raises --
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+TM_OK = 0
+_STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: "unsupported configuration",
+           4: "CUDA call failed", 5: "device barrier timeout", 6: "code or zero above 15"}
+
+EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
+           "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
+           "tm_last_launch_count")
+
+
+class TMError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+class GemmConfig(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
+                ("stages", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load the CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing; run "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, ci, csz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.tm_status_str.restype = ctypes.c_char_p
+    lib.tm_status_str.argtypes = [ci]
+    lib.tm_packed_bytes.restype = ci
+    lib.tm_packed_bytes.argtypes = [ci, ci, ci, ctypes.POINTER(csz)]
+    lib.tm_pack_weights.restype = ci
+    lib.tm_pack_weights.argtypes = [vp, vp, vp, ci, ci, ci, ctypes.POINTER(vp)]
+    lib.tm_unpack_weights.restype = ci
+    lib.tm_unpack_weights.argtypes = [vp, vp, vp, vp]
+    lib.tm_packed_info.restype = ci
+    lib.tm_packed_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci),
+                                   ctypes.POINTER(csz)]
+    lib.tm_packed_free.restype = None
+    lib.tm_packed_free.argtypes = [vp]
+    lib.tm_w4a16_gemm.restype = ci
+    lib.tm_w4a16_gemm.argtypes = [vp, vp, vp, ci, vp]
+    lib.tm_w4a16_gemm_ex.restype = ci
+    lib.tm_w4a16_gemm_ex.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
+    lib.tm_gemm_plan.restype = ci
+    lib.tm_gemm_plan.argtypes = [vp, ci, ctypes.POINTER(GemmConfig), ctypes.POINTER(GemmConfig)]
+    lib.tm_device_error.restype = ci
+    lib.tm_device_error.argtypes = [ci, ctypes.POINTER(ctypes.c_uint32)]
+    lib.tm_last_launch_count.restype = ci
+    lib.tm_last_launch_count.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(st: int, what: str):
+    if st != TM_OK:
+        raise TMError(st, what)
+
+
+def status_str(st: int) -> str:
+    return load().tm_status_str(st).decode()
+
+
+def packed_bytes(K: int, N: int, g: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().tm_packed_bytes(K, N, g, ctypes.byref(out)), "tm_packed_bytes")
+    return out.value
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+class PackedWeights:
+    """Owns a ``tm_packed`` handle (device memory on the device of ``q``)."""
+
+    def __init__(self, q: torch.Tensor, z: torch.Tensor, s: torch.Tensor, g: int):
+        lib = load()
+        K, N = q.shape
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(q.device):
+            st = lib.tm_pack_weights(_dev(q, torch.uint8, "q"), _dev(z, torch.uint8, "z"),
+                                     _dev(s, torch.float16, "s"), K, N, g, ctypes.byref(handle))
+        _check(st, "tm_pack_weights")
+        self._h = handle
+        self.K, self.N, self.g = K, N, g
+        self.device = q.device
+        b = ctypes.c_size_t()
+        _check(lib.tm_packed_info(handle, None, None, None, ctypes.byref(b)), "tm_packed_info")
+        self.nbytes = b.value
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("packed weights were freed")
+        return self._h
+
+    def unpack(self):
+        q = torch.empty((self.K, self.N), dtype=torch.uint8, device=self.device)
+        z = torch.empty((self.K // self.g, self.N), dtype=torch.uint8, device=self.device)
+        s = torch.empty((self.K // self.g, self.N), dtype=torch.float16, device=self.device)
+        with torch.cuda.device(self.device):
+            _check(load().tm_unpack_weights(self.handle, q.data_ptr(), z.data_ptr(), s.data_ptr()),
+                   "tm_unpack_weights")
+        return q, z, s
+
+    def free(self):
+        if self._h is not None:
+            load().tm_packed_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def pack(q: torch.Tensor, z: torch.Tensor, s: torch.Tensor, g: int) -> PackedWeights:
+    return PackedWeights(q, z, s, g)
+
+
+def _cfg(config) -> Optional[GemmConfig]:
+    if config is None:
+        return None
+    if isinstance(config, GemmConfig):
+        return config
+    c = GemmConfig()
+    for k, v in dict(config).items():
+        setattr(c, k, int(v))
+    return c
+
+
+def plan(w: PackedWeights, M: int, config=None) -> dict:
+    out = GemmConfig()
+    c = _cfg(config)
+    _check(load().tm_gemm_plan(w.handle, M, ctypes.byref(c) if c else None, ctypes.byref(out)), "tm_gemm_plan")
+    return out.as_dict()
+
+
+def gemm(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = None, config=None,
+         stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Y = X . dequant(W) on the GPU.
+
+    X: fp16 [M][K].  On a CUDA tensor the call is asynchronous on ``stream``
+    (default: the current stream).  On a CPU tensor (pinned for speed) X is
+    copied to the device, the product runs, and Y comes back to the host --
+    the end-to-end form of the same call.
+    """
+    if X.dim() != 2 or X.shape[1] != w.K or X.dtype != torch.float16:
+        raise ValueError("X must be fp16 [M][K]")
+    if not X.is_cuda:
+        return _gemm_host(X, w, out, config, stream)
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float16, device=X.device)
+    elif out.shape != (M, w.N) or out.dtype != torch.float16 or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA fp16 [M][N] tensor")
+    X = X.contiguous()
+    s = stream if stream is not None else torch.cuda.current_stream(X.device)
+    c = _cfg(config)
+    lib = load()
+    if c is None:
+        st = lib.tm_w4a16_gemm(X.data_ptr(), w.handle, out.data_ptr(), M, ctypes.c_void_p(s.cuda_stream))
+    else:
+        st = lib.tm_w4a16_gemm_ex(X.data_ptr(), w.handle, out.data_ptr(), M, ctypes.byref(c),
+                                  ctypes.c_void_p(s.cuda_stream))
+    _check(st, "tm_w4a16_gemm")
+    return out
+
+
+def _gemm_host(X, w, out, config, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(w.device)
+    with torch.cuda.stream(s):
+        Xd = X.to(w.device, non_blocking=True)
+        Yd = gemm(Xd, w, None, config, s)
+        if out is None:
+            out = torch.empty(Yd.shape, dtype=torch.float16, pin_memory=True)
+        out.copy_(Yd, non_blocking=True)
+    s.synchronize()
+    return out
+
+
+def device_error(clear: bool = True) -> int:
+    bits = ctypes.c_uint32()
+    st = load().tm_device_error(1 if clear else 0, ctypes.byref(bits))
+    if st not in (TM_OK, 5):
+        raise TMError(st, "tm_device_error")
+    return bits.value
+
+
+def last_launch_count() -> int:
+    return load().tm_last_launch_count()

@@ -1,0 +1,115 @@
+// C ABI entry points that are not tied to one kernel: argument checks, the
+// choice between the decode and the prefill kernel, status strings and the
+// device error word.
+#include <cstdint>
+#include <mutex>
+
+#include "tm_common.cuh"
+
+namespace w4 {
+
+namespace {
+thread_local int t_launches = 0;
+std::mutex g_mu;
+int g_sms[64] = {0};
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+int num_sms(int device) {
+  if (device < 0 || device >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[device]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || v <= 0) v = 148;
+    g_sms[device] = v;
+  }
+  return g_sms[device];
+}
+
+void set_launch_count(int n) { t_launches = n; }
+
+// Largest M served by the decode kernel when the path is automatic.
+constexpr int kDecodeMaxM = 64;
+constexpr int kAutoDecodeMaxM = 32;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static tm_status plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out) {
+  int path = cfg ? cfg->path : 0;
+  if (path == 0) path = M <= kAutoDecodeMaxM ? 1 : 2;
+  if (path == 1) {
+    if (M > kDecodeMaxM) return TM_ERR_UNSUPPORTED;
+    return plan_decode(p, M, cfg, out);
+  }
+  if (path == 2) return plan_prefill(p, M, cfg, out);
+  return TM_ERR_INVALID_ARG;
+}
+
+}  // namespace w4
+
+using namespace w4;
+
+extern "C" const char* tm_status_str(tm_status s) {
+  switch (s) {
+    case TM_OK: return "ok";
+    case TM_ERR_INVALID_ARG: return "invalid argument";
+    case TM_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case TM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case TM_ERR_CUDA: return "CUDA call failed";
+    case TM_ERR_DEVICE_TIMEOUT: return "device barrier timeout";
+    case TM_ERR_BAD_CODE: return "code or zero above 15";
+  }
+  return "unknown status";
+}
+
+extern "C" tm_status tm_gemm_plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out) {
+  if (!p || !out || M < 0) return TM_ERR_INVALID_ARG;
+  return plan(p, M > 0 ? M : 1, cfg, out);
+}
+
+extern "C" tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config* cfg,
+                                      void* stream) {
+  t_launches = 0;
+  if (!p || M < 0) return TM_ERR_INVALID_ARG;
+  if (M == 0) return TM_OK;
+  if (!X || !Y) return TM_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Y)) return TM_ERR_ALIGNMENT;
+  tm_gemm_config c;
+  tm_status st = plan(p, M, cfg, &c);
+  if (st != TM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (c.path == 1) return launch_decode(X, p, Y, M, c, s);
+  return launch_prefill(X, p, Y, M, c, s);
+}
+
+extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void* stream) {
+  return tm_w4a16_gemm_ex(X, p, Y, M, nullptr, stream);
+}
+
+extern "C" tm_status tm_device_error(int clear, uint32_t* bits) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return TM_ERR_CUDA;
+  uint32_t a = 0, b = 0, c = 0;
+  if (pack_error_bits(&a, clear != 0) != cudaSuccess || decode_error_bits(&b, clear != 0) != cudaSuccess ||
+      prefill_error_bits(&c, clear != 0) != cudaSuccess)
+    return TM_ERR_CUDA;
+  const uint32_t v = (a | b | c) & kErrTimeout;
+  if (bits) *bits = v;
+  return v ? TM_ERR_DEVICE_TIMEOUT : TM_OK;
+}
+
+extern "C" int tm_last_launch_count(void) { return t_launches; }
