@@ -1,0 +1,517 @@
+"""Benchmark of the W4A16 GEMM on GB300: one JSON line on rank 0.
+
+Default workload (the metric's headline configuration): the Llama-3-8B decode
+linear layers -- qkv (4096x6144), o_proj (4096x4096), gate_up (4096x28672),
+down (14336x4096) -- at M in {1, 8, 16, 32}, g = 128.  One step = those 16
+GEMMs, each with its own packed weights, X and Y (440 MB of distinct packed
+weights per step, more than the 129 MB L2, so every step streams its weights
+from HBM).  A step is captured once as a CUDA graph and replayed.
+
+  value     = algorithmic bytes of the step / device time per step (GB/s),
+              summed over all ranks (replicas) for --gpus N.
+  roofline  = the decode kernel against the measured HBM copy bandwidth.
+  e2e       = the same metric through the public call with host buffers:
+              per GEMM, pinned X -> device, product, Y -> pinned host.
+  cpu_baseline = the fp64 oracle on a bounded column sample of the same
+              workload, extrapolated to the full step, on the host cores.
+
+--workload prefill runs the Llama-3-8B prefill shapes (M in {128,1024,4096},
+TFLOP/s against the measured tensor peak) instead.
+--impl reference times the oracle as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "W4A16 GEMM GB/s (M≤32) & TFLOP/s (M≥128), % of roofline, Llama-3 shapes"
+WORKLOADS = {
+    "decode": {"idx": 1, "unit": "GB/s", "bound": "hbm",
+               "name": "llama3-8b decode linears: qkv/o_proj/gate_up/down x M in {1,8,16,32}, g=128"},
+    "prefill": {"idx": 2, "unit": "TFLOP/s", "bound": "tensor",
+                "name": "llama3-8b prefill linears: qkv/o_proj/gate_up/down x M in {128,1024,4096}, g=128"},
+}
+KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "prefill": ["prefill.cu", "tm_common.cuh"]}
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def algorithmic_bytes(M, K, N, g):
+    G = K // g
+    return K * N // 2 + G * N * 2 + G * N // 2 + 2 * M * K + 2 * M * N
+
+
+def flops(M, K, N):
+    return 2 * M * N * K
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "of measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "of fallback"}
+
+
+def kernel_hash(kind):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "w4a16_quantized_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(kind, workload):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary,
+    or None when there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_kernel_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    d = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                d[k.strip()] = v.strip()
+    if d.get("kernel_source_sha") != kernel_hash(kind):
+        return None
+    try:
+        return float(d["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value, world):
+    """Max over ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units, world, t_max_s):
+    """Whole-job throughput: units every rank processed / slowest rank's time."""
+    return per_rank_units * world / t_max_s
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU arm ---
+
+class Workload:
+    def __init__(self, kind, device, copies=1):
+        import numpy as np
+        import torch
+
+        from w4a16_quantized_gemm_gb300 import binding, synth
+
+        self.kind = kind
+        self.cases = synth.workload(WORKLOADS[kind]["idx"])
+        self.items = []
+        weights_cache = {}
+        for c in self.cases:
+            key = (c.K, c.N, c.g)
+            if key not in weights_cache:
+                weights_cache[key] = synth.weights(c.K, c.N, c.g)
+            q, z, s, _ = weights_cache[key]
+            qd = torch.from_numpy(q).to(device)
+            zd = torch.from_numpy(z).to(device)
+            sd = torch.from_numpy(s.view(np.uint16)).to(device).view(torch.float16)
+            w = binding.pack(qd, zd, sd, c.g)
+            del qd, zd, sd
+            Xh = synth.activations(c.M, c.K, None, 0, tag=f"/N{c.N}/g{c.g}")
+            X = torch.from_numpy(Xh.view(np.uint16)).to(device).view(torch.float16)
+            Y = torch.empty((c.M, c.N), dtype=torch.float16, device=device)
+            self.items.append({"case": c, "w": w, "X": X, "Y": Y, "Xh": Xh,
+                               "bytes": algorithmic_bytes(c.M, c.K, c.N, c.g), "flops": flops(c.M, c.K, c.N),
+                               "plan": binding.plan(w, c.M)})
+        self.step_bytes = sum(i["bytes"] for i in self.items)
+        self.step_flops = sum(i["flops"] for i in self.items)
+        self.weight_bytes = sum(i["w"].nbytes for i in self.items)
+
+    def launch_all(self, stream, events=None):
+        from w4a16_quantized_gemm_gb300 import binding
+        n = 0
+        for k, it in enumerate(self.items):
+            if events is not None:
+                events[k].record(stream)
+            binding.gemm(it["X"], it["w"], out=it["Y"], stream=stream)
+            n += binding.last_launch_count()
+        if events is not None:
+            events[len(self.items)].record(stream)
+        return n
+
+
+def run_gpu(args, rank, world, local):
+    import torch
+
+    from w4a16_quantized_gemm_gb300 import binding
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    wl = Workload(args.workload, device)
+    spec = WORKLOADS[args.workload]
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+
+    # capture one step as a graph; also one graph per GEMM for the per-launch timing
+    with torch.cuda.stream(stream):
+        wl.launch_all(stream)  # warm the kernels (attributes, module load) before capture
+    stream.synchronize()
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=stream):
+        launches_per_step = wl.launch_all(torch.cuda.current_stream())
+    g_each = []
+    for it in wl.items:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            binding.gemm(it["X"], it["w"], out=it["Y"], stream=torch.cuda.current_stream())
+        g_each.append(g)
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g_plain.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_sampler0 = time.time()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for k in range(args.steps):
+            g_plain.replay()
+            evs[k + 1].record(stream)
+    stream.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [evs[k].elapsed_time(evs[k + 1]) for k in range(args.steps)]
+    t_total_ms = evs[0].elapsed_time(evs[-1])
+    # keep the same load running until the sampler has seen >= 1.5 s of it
+    extra = 0
+    with torch.cuda.stream(stream):
+        while time.time() - t_sampler0 < 1.5:
+            for _ in range(200):
+                g_plain.replay()
+                extra += 1
+            stream.synchronize()
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = f"timed region + {extra} untimed steps of the same workload"
+
+    t_max_s = reduce_max(t_total_ms / 1e3, world)
+
+    # Per-launch kernel time: the step's GEMMs in order, one graph launch each,
+    # bracketed by events; a GPU sleep first lets the host queue all of it so
+    # that no host gap falls inside a bracket.
+    reps = 20
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in wl.items]
+          for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            torch.cuda._sleep(20_000_000)
+            for k, g in enumerate(g_each):
+                ev[r][k][0].record(stream)
+                g.replay()
+                ev[r][k][1].record(stream)
+    stream.synchronize()
+    per_gemm_ms = [statistics.mean(ev[r][k][0].elapsed_time(ev[r][k][1]) for r in range(reps))
+                   for k in range(len(wl.items))]
+    detail = []
+    for k, it in enumerate(wl.items):
+        ms = per_gemm_ms[k]
+        c = it["case"]
+        rt = max(it["bytes"] / (peaks["hbm_gbs"] * 1e9), it["flops"] / (peaks["bf16_tflops"] * 1e12))
+        detail.append({"gemm": c.name, "us": round(ms * 1e3, 2),
+                       "GB/s": round(it["bytes"] / (ms * 1e-3) / 1e9, 1),
+                       "TFLOP/s": round(it["flops"] / (ms * 1e-3) / 1e12, 1),
+                       "roofline_frac": round(rt / (ms * 1e-3), 3), "plan": it["plan"]})
+    kernel_s = sum(per_gemm_ms) * 1e-3
+
+    if spec["unit"] == "GB/s":
+        per_rank_units = wl.step_bytes * args.steps / 1e9
+        achieved = wl.step_bytes / kernel_s / 1e9
+        peak = peaks["hbm_gbs"]
+        traffic = read_traffic("decode", "llama3_8b_decode")
+        unit_kernel = "GB/s"
+    else:
+        per_rank_units = wl.step_flops * args.steps / 1e12
+        achieved = wl.step_flops / kernel_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        traffic = read_traffic("prefill", "llama3_8b_prefill")
+        unit_kernel = "TFLOP/s"
+    value = aggregate(per_rank_units, world, t_max_s)
+
+    e2e = run_e2e(wl, args, spec) if rank == 0 else None
+    cpu = cpu_baseline(wl, args.cpu_seconds) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": spec["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": spec["name"], "gemms_per_step": len(wl.items),
+                   "bytes_per_step": wl.step_bytes, "flops_per_step": wl.step_flops,
+                   "packed_weight_bytes_per_step": wl.weight_bytes,
+                   "accumulate": "f32", "launch": "one CUDA graph per step (16 kernel nodes)",
+                   "l2": "inputs larger than L2: every GEMM of a step has its own weights (>129 MB per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
+                     "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peaks["source"],
+                     "kernel": "decode_kernel" if spec["bound"] == "hbm" else "prefill_kernel",
+                     "basis": "algorithmic units of the step's launches / sum of their mean launch "
+                              "durations (CUDA events around each launch, 20 passes over the step)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "detail": detail,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(wl, args, spec):
+    """Public call with host buffers: per GEMM, pinned X in, product, pinned Y out."""
+    import numpy as np
+    import torch
+
+    from w4a16_quantized_gemm_gb300 import binding
+
+    hostX = [torch.from_numpy(it["Xh"].view(np.uint16)).view(torch.float16).pin_memory() for it in wl.items]
+    hostY = [torch.empty(tuple(it["Y"].shape), dtype=torch.float16, pin_memory=True) for it in wl.items]
+    h2d = sum(x.numel() * 2 for x in hostX)
+    d2h = sum(y.numel() * 2 for y in hostY)
+    steps = max(3, min(args.steps, 200))
+    for _ in range(2):
+        for it, x, y in zip(wl.items, hostX, hostY):
+            binding.gemm(x, it["w"], out=y)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for it, x, y in zip(wl.items, hostX, hostY):
+            binding.gemm(x, it["w"], out=y)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    units = (wl.step_bytes / 1e9) if spec["unit"] == "GB/s" else (wl.step_flops / 1e12)
+    return {"value": round(units * steps / dt, 2), "unit": spec["unit"], "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt * 1e3 / steps, 3),
+            "timing": "host wall clock; each call copies X in, runs, copies Y out and synchronises"}
+
+
+# ------------------------------------------------------------ CPU baseline ---
+
+def _oracle_sample(cases_weights, cols, threads):
+    """Time the oracle on the first `cols` columns of every GEMM; returns
+    (seconds, extrapolated seconds for the full step)."""
+    import numpy as np
+
+    import oracle
+    t_sample = 0.0
+    t_full = 0.0
+    for (c, q, z, s, X) in cases_weights:
+        n = min(c.N, cols)
+        qs, zs, ss = (np.ascontiguousarray(a[:, :n]) for a in (q, z, s))
+        t0 = time.perf_counter()
+        oracle.gemm(X, qs, zs, ss, c.g, threads=threads)
+        dt = time.perf_counter() - t0
+        t_sample += dt
+        t_full += dt * c.N / n
+    return t_sample, t_full
+
+
+def _cases_with_weights(kind):
+    from w4a16_quantized_gemm_gb300 import synth
+    out = []
+    cache = {}
+    for c in synth.workload(WORKLOADS[kind]["idx"]):
+        key = (c.K, c.N, c.g)
+        if key not in cache:
+            cache[key] = synth.weights(c.K, c.N, c.g)
+        q, z, s, _ = cache[key]
+        X = synth.activations(c.M, c.K, None, 0, tag=f"/N{c.N}/g{c.g}")
+        out.append((c, q, z, s, X))
+    return out
+
+
+def _calibrated_cols(cw, budget_s, threads):
+    t, _ = _oracle_sample(cw, 16, threads)
+    cols = int(16 * budget_s / max(t, 1e-6))
+    return max(16, min(cols // 16 * 16, max(c.N for (c, *_rest) in cw)))
+
+
+def cpu_baseline(wl, budget_s):
+    import oracle
+    threads = oracle.default_threads()
+    cw = _cases_with_weights(wl.kind)
+    cols = _calibrated_cols(cw, budget_s, threads)
+    t_sample, t_full = _oracle_sample(cw, cols, threads)
+    spec = WORKLOADS[wl.kind]
+    units = wl.step_bytes / 1e9 if spec["unit"] == "GB/s" else wl.step_flops / 1e12
+    return {"value": round(units / t_full, 4), "unit": spec["unit"], "cores": threads, "kind": "oracle",
+            "sample": f"every GEMM of one step on its first {cols} output columns (all M rows, full K); "
+                      f"{t_sample:.1f} s measured, scaled by N/{cols} per GEMM to a full step "
+                      f"({t_full:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    from w4a16_quantized_gemm_gb300 import synth
+    spec = WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    cw = _cases_with_weights(args.workload)
+    per_step = max(0.5, min(4.0, 120.0 / max(1, args.steps + args.warmup)))
+    cols = _calibrated_cols(cw, per_step, threads)
+    for _ in range(args.warmup):
+        _oracle_sample(cw, cols, threads)
+    t_s = 0.0
+    t_full = 0.0
+    for _ in range(args.steps):
+        a, b = _oracle_sample(cw, cols, threads)
+        t_s += a
+        t_full += b
+    bytes_step = sum(algorithmic_bytes(c.M, c.K, c.N, c.g) for (c, *_r) in cw)
+    flops_step = sum(flops(c.M, c.K, c.N) for (c, *_r) in cw)
+    units = bytes_step / 1e9 if spec["unit"] == "GB/s" else flops_step / 1e12
+    value = units * args.steps / t_full
+    sample = (f"each step: every GEMM on its first {cols} output columns (all M rows, full K), "
+              f"scaled by N/{cols} per GEMM to a full step")
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": spec["unit"],
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(t_full * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": spec["name"], "gemms_per_step": len(cw)},
+           "cpu_baseline": {"value": round(value, 4), "unit": spec["unit"], "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": spec["unit"], "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world != args.gpus and "RANK" in os.environ:
+        p.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
