@@ -15,16 +15,20 @@ namespace w4 {
 
 static __device__ uint32_t s_err_pack;
 
-// One thread per 32-bit code word.  Word index = ((nt*KT + kt)*32 + lane)*4 + st.
-__global__ void pack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, int KT, long long nwords,
+// One thread per 32-bit code word.
+// Word index = (((sg*NT + nt)*UPS + u)*32 + lane)*4 + st.
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, int NT, int UPS, long long nwords,
                                   uint32_t* __restrict__ out) {
   long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= nwords) return;
   const int st = (int)(w & 3);
   const int lane = (int)((w >> 2) & 31);
   const long long unit = w >> 7;
-  const int kt = (int)(unit % KT);
-  const int nt = (int)(unit / KT);
+  const int u = (int)(unit % UPS);
+  const long long rest = unit / UPS;
+  const int nt = (int)(rest % NT);
+  const int sg = (int)(rest / NT);
+  const int kt = sg * UPS + u;
   const int gr = lane >> 2, t = lane & 3;
   uint32_t word = 0;
   bool bad = false;
@@ -48,15 +52,16 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ q, int K, int N, i
   out[w] = word;
 }
 
-// One thread per (nt, grp, gr): the fp16 pair (s[n0+gr], s[n0+gr+8]).
-__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int Gk, int N, int G, long long npairs,
+// One thread per (sg, nt, group of the pair, gr): the fp16 pair (s[n0+gr], s[n0+gr+8]).
+__global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int Gk, int N, int NT, long long npairs,
                                    uint32_t* __restrict__ out) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= npairs) return;
   const int gr = (int)(i & 7);
-  const long long rest = i >> 3;
-  const int grp = (int)(rest % G);
-  const int nt = (int)(rest / G);
+  const int gi = (int)((i >> 3) & 1);
+  const long long rest = i >> 4;
+  const int nt = (int)(rest % NT);
+  const int grp = 2 * (int)(rest / NT) + gi;
   uint32_t lo = 0, hi = 0;
   const int n = nt * 16 + gr;
   if (grp < Gk) {
@@ -66,15 +71,15 @@ __global__ void pack_scales_kernel(const uint16_t* __restrict__ s, int Gk, int N
   out[i] = lo | (hi << 16);
 }
 
-// One thread per zero byte: (nt, pair sg, byte b) -> group 2*sg + (b >> 3), row b & 7.
-__global__ void pack_zeros_kernel(const uint8_t* __restrict__ z, int Gk, int N, int Gh, long long nbytes,
+// One thread per zero byte: (sg, nt, byte b) -> group 2*sg + (b >> 3), row b & 7.
+__global__ void pack_zeros_kernel(const uint8_t* __restrict__ z, int Gk, int N, int NT, long long nbytes,
                                   uint8_t* __restrict__ out) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= nbytes) return;
   const int b = (int)(i & 15);
   const long long rest = i >> 4;
-  const int sg = (int)(rest % Gh);
-  const int nt = (int)(rest / Gh);
+  const int nt = (int)(rest % NT);
+  const int sg = (int)(rest / NT);
   const int grp = 2 * sg + (b >> 3);
   const int gr = b & 7;
   const int n = nt * 16 + gr;
@@ -88,7 +93,7 @@ __global__ void pack_zeros_kernel(const uint8_t* __restrict__ z, int Gk, int N, 
 }
 
 // Inverse: one thread per (k, n) code.
-__global__ void unpack_codes_kernel(const uint32_t* __restrict__ words, int K, int N, int KT,
+__global__ void unpack_codes_kernel(const uint32_t* __restrict__ words, int K, int N, int NT, int UPS,
                                     uint8_t* __restrict__ q) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)K * N) return;
@@ -97,18 +102,20 @@ __global__ void unpack_codes_kernel(const uint32_t* __restrict__ words, int K, i
   const int kt = k / kUnitK, kk = k % kUnitK, t = kk >> 4, st = (kk >> 2) & 3, j = kk & 3;
   const int lane = gr * 4 + t;
   const int nib = hirow + 2 * (j >> 1) + 4 * (j & 1);
-  const uint32_t w = words[(((size_t)nt * KT + kt) * 32 + lane) * 4 + st];
+  const int sg = kt / UPS, u = kt % UPS;
+  const uint32_t w = words[((((size_t)sg * NT + nt) * UPS + u) * 32 + lane) * 4 + st];
   q[i] = (uint8_t)((w >> (4 * nib)) & 15);
 }
 
 __global__ void unpack_meta_kernel(const uint16_t* __restrict__ sp, const uint8_t* __restrict__ zp, int Gk, int N,
-                                   int G, uint8_t* __restrict__ z, uint16_t* __restrict__ s) {
+                                   int NT, uint8_t* __restrict__ z, uint16_t* __restrict__ s) {
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)Gk * N) return;
   const int grp = (int)(i / N), n = (int)(i % N);
   const int nt = n >> 4, r = n & 15, gr = r & 7, hirow = r >> 3;
-  s[i] = sp[((size_t)nt * G + grp) * 16 + 2 * gr + hirow];
-  const uint8_t b = zp[((size_t)nt * (G / 2) + grp / 2) * 16 + (grp & 1) * 8 + gr];
+  const int sg = grp >> 1;
+  s[i] = sp[(((size_t)sg * NT + nt) * 2 + (grp & 1)) * 16 + 2 * gr + hirow];
+  const uint8_t b = zp[((size_t)sg * NT + nt) * 16 + (grp & 1) * 8 + gr];
   z[i] = hirow ? (b >> 4) : (b & 15);
 }
 
@@ -124,17 +131,21 @@ cudaError_t pack_error_bits(uint32_t* bits, bool clear) {
   return e;
 }
 
-static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t d0, uint64_t d1,
-                      uint64_t stride1_bytes, uint32_t b0, uint32_t b1) {
+// Tensor map without swizzle: dims[0] innermost, strides in bytes for dims 1..rank-1.
+static bool encode_nd(CUtensorMap* map, CUtensorMapDataType dt, void* base, int rank, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {d0, d1};
-  cuuint64_t strides[1] = {stride1_bytes};
-  cuuint32_t box[2] = {b0, b1};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(map, dt, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  CUresult r = fn(map, dt, (cuuint32_t)rank, base, d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -180,13 +191,13 @@ extern "C" tm_status tm_pack_weights(const uint8_t* q, const uint8_t* z, const u
   const int B = 256;
   const long long nwords = (long long)L.NT * L.KT * 128;
   const long long npairs = (long long)L.NT * L.G * 8;
-  const long long nzb = (long long)L.NT * (L.G / 2) * 16;
+  const long long nzb = (long long)L.NT * L.NSG * 16;
   if (e == cudaSuccess) {
-    pack_codes_kernel<<<grid_for(nwords, B), B>>>(q, K, N, L.KT, nwords,
+    pack_codes_kernel<<<grid_for(nwords, B), B>>>(q, K, N, L.NT, L.UPS, nwords,
                                                   reinterpret_cast<uint32_t*>(p->base + L.codes_off));
-    pack_scales_kernel<<<grid_for(npairs, B), B>>>(s, K / g, N, L.G, npairs,
+    pack_scales_kernel<<<grid_for(npairs, B), B>>>(s, K / g, N, L.NT, npairs,
                                                    reinterpret_cast<uint32_t*>(p->base + L.scales_off));
-    pack_zeros_kernel<<<grid_for(nzb, B), B>>>(z, K / g, N, L.G / 2, nzb, p->base + L.zeros_off);
+    pack_zeros_kernel<<<grid_for(nzb, B), B>>>(z, K / g, N, L.NT, nzb, p->base + L.zeros_off);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -201,15 +212,23 @@ extern "C" tm_status tm_pack_weights(const uint8_t* q, const uint8_t* z, const u
     delete p;
     return TM_ERR_BAD_CODE;
   }
-  // Tensor maps for the prefill kernel: codes as u32 rows of one n-tile
-  // (box = one 64-k unit x 16 n-tiles), scales (box = one group x 16 n-tiles),
-  // zeros (box = one pair of groups x 16 n-tiles).
-  bool ok = encode_2d(&p->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, p->base + L.codes_off, (uint64_t)L.KT * 128,
-                      (uint64_t)L.NT, (uint64_t)L.KT * kUnitBytes, 128, 16) &&
-            encode_2d(&p->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, p->base + L.scales_off, (uint64_t)L.G * 16,
-                      (uint64_t)L.NT, (uint64_t)L.G * 32, 16, 16) &&
-            encode_2d(&p->tm_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->base + L.zeros_off, (uint64_t)(L.G / 2) * 16,
-                      (uint64_t)L.NT, (uint64_t)(L.G / 2) * 16, 16, 16);
+  // Tensor maps for the prefill kernel, one box = one 64-k unit (or its
+  // group's scales / the pair's zeros) of 16 consecutive n-tiles:
+  //   codes  u32 {128, UPS, NT, NSG}   box {128, 1, 16, 1}
+  //   scales u16 {16, 2, NT, NSG}      box {16, 1, 16, 1}
+  //   zeros  u8  {16, NT, NSG}         box {16, 16, 1}
+  const uint64_t cd[4] = {128, (uint64_t)L.UPS, (uint64_t)L.NT, (uint64_t)L.NSG};
+  const uint64_t cs[3] = {kUnitBytes, (uint64_t)L.UPS * kUnitBytes, (uint64_t)L.NT * L.UPS * kUnitBytes};
+  const uint32_t cb[4] = {128, 1, 16, 1};
+  const uint64_t sd[4] = {16, 2, (uint64_t)L.NT, (uint64_t)L.NSG};
+  const uint64_t ss[3] = {32, 64, (uint64_t)L.NT * 64};
+  const uint32_t sb[4] = {16, 1, 16, 1};
+  const uint64_t zd[3] = {16, (uint64_t)L.NT, (uint64_t)L.NSG};
+  const uint64_t zs[2] = {16, (uint64_t)L.NT * 16};
+  const uint32_t zb[3] = {16, 16, 1};
+  bool ok = encode_nd(&p->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, p->base + L.codes_off, 4, cd, cs, cb) &&
+            encode_nd(&p->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, p->base + L.scales_off, 4, sd, ss, sb) &&
+            encode_nd(&p->tm_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->base + L.zeros_off, 3, zd, zs, zb);
   if (!ok) {
     cudaFree(p->base);
     delete p;
@@ -226,9 +245,9 @@ extern "C" tm_status tm_unpack_weights(const tm_packed* p, uint8_t* q, uint8_t* 
   const long long nq = (long long)L.K * L.N;
   const long long nm = (long long)(L.K / L.g) * L.N;
   unpack_codes_kernel<<<grid_for(nq, B), B>>>(reinterpret_cast<const uint32_t*>(p->base + L.codes_off), L.K, L.N,
-                                              L.KT, q);
+                                              L.NT, L.UPS, q);
   unpack_meta_kernel<<<grid_for(nm, B), B>>>(reinterpret_cast<const uint16_t*>(p->base + L.scales_off),
-                                             p->base + L.zeros_off, L.K / L.g, L.N, L.G, z, s);
+                                             p->base + L.zeros_off, L.K / L.g, L.N, L.NT, z, s);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return e == cudaSuccess ? TM_OK : TM_ERR_CUDA;

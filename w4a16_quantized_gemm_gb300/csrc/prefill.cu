@@ -50,7 +50,7 @@ struct PrefillShape {
 
 struct PrefillParams {
   __half* Y;
-  int M, N, NT, KT, G, g;
+  int M, N, NT, KT, G, g, UPS;
   int kb_total;  // 64-k blocks
 };
 
@@ -126,9 +126,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         const int grp = kb * kBK / P.g;
         mbar_expect_tx(full, SH::TX);
         tma_load_2d(st + SH::A_OFF, &tmX, kb * kBK, m0, full);
-        tma_load_2d(st + SH::C_OFF, &tmC, kb * (kUnitBytes / 4), nt0, full);
-        tma_load_2d(st + SH::S_OFF, &tmS, grp * 16, nt0, full);
-        tma_load_2d(st + SH::Z_OFF, &tmZ, (grp >> 1) * 16, nt0, full);
+        tma_load_4d(st + SH::C_OFF, &tmC, 0, kb % P.UPS, nt0, kb / P.UPS, full);
+        tma_load_4d(st + SH::S_OFF, &tmS, 0, grp & 1, nt0, grp >> 1, full);
+        tma_load_3d(st + SH::Z_OFF, &tmZ, 0, nt0, grp >> 1, full);
         ++issued;
       }
       for (int i = max(0, issued - STAGES); i < issued; ++i)
@@ -331,6 +331,7 @@ tm_status launch_prefill(const void* X, const tm_packed* p, void* Y, int M, cons
   P.KT = L.KT;
   P.G = L.G;
   P.g = L.g;
+  P.UPS = L.UPS;
   P.kb_total = L.Kp / kBK;
   tm_status st = TM_ERR_UNSUPPORTED;
   if (c.tile_n == 256 && c.stages == 3) st = launch_t<256, 3>(tmX, p, P, stream);

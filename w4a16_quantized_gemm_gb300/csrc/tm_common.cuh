@@ -25,13 +25,16 @@
 // the step is permuted the same way on X (slot 2t -> 4t, 2t+1 -> 4t+1,
 // 2t+8 -> 4t+2, 2t+9 -> 4t+3).
 //
-// Regions (one allocation, each 1024-byte aligned):
-//   codes  [NT][KT][512 B]          NT = N/16, KT = Kp/64
-//   scales [NT][G][16 x fp16]       element 2*gr + h = s[grp][n0 + gr + 8h]
-//   zeros  [NT][G/2][16 B]          byte (grp&1)*8 + gr: low nibble z of row gr,
-//                                   high nibble z of row gr+8
-// Kp is K rounded up to 2g (an even number of groups G = Kp/g); the padding
-// groups hold zero codes, zeros and scales.
+// Regions (one allocation, each 1024-byte aligned), ordered by pairs of groups
+// ("super-groups", SG = 2g values of k) first, so that the codes, scales and
+// zeros one CTA needs for one super-group of consecutive n-tiles are each a
+// single contiguous run:
+//   codes  [NSG][NT][UPS][512 B]     UPS = 2g/64 units per super-group
+//   scales [NSG][NT][2][16 x fp16]   element 2*gr + h = s[grp][n0 + gr + 8h]
+//   zeros  [NSG][NT][16 B]           byte (grp&1)*8 + gr: low nibble z of row gr,
+//                                    high nibble z of row gr+8
+// NT = N/16; NSG = Kp/(2g), with Kp = K rounded up to 2g; the padding group
+// holds zero codes, zeros and scales.
 // ---------------------------------------------------------------------------
 
 namespace w4 {
@@ -41,7 +44,7 @@ constexpr int kUnitBytes = 512;
 
 struct Layout {
   int K, N, g;
-  int Kp, NT, KT, G;
+  int Kp, NT, KT, G, NSG, UPS;
   size_t codes_off, scales_off, zeros_off, total;
 };
 
@@ -54,13 +57,15 @@ inline Layout make_layout(int K, int N, int g) {
   L.NT = N / 16;
   L.KT = L.Kp / kUnitK;
   L.G = L.Kp / g;
+  L.NSG = L.G / 2;
+  L.UPS = 2 * g / kUnitK;
   auto al = [](size_t v) { return (v + 1023) & ~size_t(1023); };
   L.codes_off = 0;
   size_t codes = (size_t)L.NT * L.KT * kUnitBytes;
   L.scales_off = al(codes);
   size_t scales = (size_t)L.NT * L.G * 32;
   L.zeros_off = al(L.scales_off + scales);
-  size_t zeros = (size_t)L.NT * (L.G / 2) * 16;
+  size_t zeros = (size_t)L.NT * L.NSG * 16;
   L.total = al(L.zeros_off + zeros);
   return L;
 }
@@ -189,6 +194,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -287,15 +309,30 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split form: arrive early, wait before the first access to another CTA's
+// shared memory (it must have started running).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// ---- programmatic dependent launch ------------------------------------------
+// Wait until the preceding grid in the stream finished and its writes are
+// visible (no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid in the stream to begin launching.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- tcgen05 --------------------------------------------------------------
