@@ -6,16 +6,19 @@
 // keeps the idea and changes the machinery:
 //   * one elected producer thread streams each CTA's packed codes, scales and
 //     zeros into a shared-memory ring with three 1-D bulk async copies
-//     (cp.async.bulk) per stage, and the CTA's slice of X with 2-D TMA
-//     (128-byte swizzle); consumers wait on mbarriers;
+//     (cp.async.bulk) per stage, and the CTA's slice of X with 2-D TMA;
+//     consumers wait on mbarriers;
 //   * because the packer already stored every 32-bit word in mma.m16n8k16
 //     A-fragment order, one 16-byte shared load per lane gives four MMA
 //     fragments -- no ldmatrix and no runtime swizzle;
-//   * dequantisation is 9 integer/half instructions per 8 weights: LOP3
-//     mask-and-OR with the 0x6400 (1024.0) pattern turns nibbles into
-//     1024 + q (or 1024 + 16 q), one HSUB2/HFMA2 gives q - z exactly; the
-//     fp16 scale multiplies the fp32 per-group partial sum instead of the
-//     weight, so no weight is rounded;
+//   * dequantisation: LOP3 mask-and-OR with the 0x6400 (1024.0) pattern turns
+//     nibbles into 1024 + q (or 1024 + 16 q); either one HSUB2/HFMA2 per pair
+//     gives q - z exactly (9 instructions per 8 weights), or the raw values go
+//     straight into the MMA and the zero point and offset are removed once per
+//     group with the sum of x (5 instructions per 8 weights plus one product
+//     with an all-ones fragment per step, shared by the warp's n-tiles); the
+//     fp16 scale multiplies the fp32 per-group partial sum, so no weight is
+//     rounded;
 //   * W^T is the MMA's A operand (16 output columns per fragment) and X^T its
 //     B operand (8 rows of X per n8 tile), so one dequantised fragment serves
 //     every 8 rows of X;
@@ -43,22 +46,11 @@ struct DecodeParams {
   int nsg_total;   // pairs of groups
   int sg_per_cta;  // pairs of groups per CTA of a cluster
   int stages;
-  uint32_t stage_bytes;
-  uint32_t r_off;    // offset of the reduction buffer
-  uint32_t bar_off;  // offset of the barriers
-};
-
-template <int MT, int WN, int NW, int UPS>
-struct DecodeShape {
-  static constexpr int CN = NW * WN;   // n-tiles per CTA
-  static constexpr int CNN = CN * 16;  // columns per CTA
-  static constexpr uint32_t X_BYTES = UPS * MT * 1024;
-  static constexpr uint32_t C_BYTES = CN * UPS * kUnitBytes;
-  static constexpr uint32_t S_BYTES = CN * 64;
-  static constexpr uint32_t Z_BYTES = CN * 16;
-  static constexpr uint32_t STAGE_RAW = X_BYTES + C_BYTES + S_BYTES + Z_BYTES;
-  static constexpr uint32_t STAGE = (STAGE_RAW + 1023) & ~1023u;
-  static constexpr uint32_t R_BYTES = MT * 8 * CNN * 4;  // [S][MT*8][span] floats
+  uint32_t x_unit;       // bytes of X per 64-k unit in a stage
+  uint32_t c_off;        // offset of the codes in a stage
+  uint32_t stage_bytes;  // bytes per stage (1024-aligned)
+  uint32_t r_off;        // offset of the reduction buffer
+  uint32_t bar_off;      // offset of the barriers
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -72,12 +64,18 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <int MT, int WN, int NW, int UPS>
+// MT: 8-row tiles of X (M <= 8 MT); WN: n-tiles per consumer warp; NW:
+// consumer warps; UPS: 64-k units per stage (2g/64); XP: X stored as M plain
+// rows (M < 8) instead of 8 MT swizzled rows.
+template <int MT, int WN, int NW, int UPS, bool XP>
 __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                const DecodeParams P) {
-  using SH = DecodeShape<MT, WN, NW, UPS>;
-  constexpr int CN = SH::CN;
-  constexpr int UPG = UPS / 2;  // units (of 64 k) per group
+  constexpr int CN = NW * WN;    // n-tiles per CTA
+  constexpr int CNN = CN * 16;   // columns per CTA
+  constexpr int UPG = UPS / 2;   // units (of 64 k) per group
+  constexpr int NACC = MT == 1 ? 2 : 1;  // independent accumulator chains
+  // Raw-code products pay off when the all-ones product is shared by several tiles.
+  constexpr bool kRaw = WN >= 2 && MT < 4 * WN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -95,6 +93,8 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
   const uint32_t bar_empty = bar_full + 8 * stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + 16 * stages);
   float* red = reinterpret_cast<float*>(smem + P.r_off);
+  const uint32_t s_off = P.c_off + CN * UPS * kUnitBytes;
+  const uint32_t z_off = s_off + CN * 64;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -115,19 +115,17 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
     if (lane == 0) {
       prefetch_tmap(&tmX);
       const int nvalid = min(CN, P.NT - nt0);
-      const uint32_t tx = SH::X_BYTES + (uint32_t)nvalid * (UPS * kUnitBytes + 64 + 16);
+      const uint32_t tx = UPS * P.x_unit + (uint32_t)nvalid * (UPS * kUnitBytes + 64 + 16);
       auto issue_weights = [&](int i) {
         const int slot = i % stages;
         const int sg = sg_begin + i;
         const uint32_t full = bar_full + 8 * slot;
-        const uint32_t c_dst = base + slot * P.stage_bytes + SH::X_BYTES;
-        const uint32_t s_dst = c_dst + SH::C_BYTES;
-        const uint32_t z_dst = s_dst + SH::S_BYTES;
+        const uint32_t st = base + slot * P.stage_bytes;
         // one contiguous run each: codes, scales and zeros of n-tiles nt0.. for super-group sg
         const size_t row = (size_t)sg * P.NT + nt0;
-        bulk_g2s(c_dst, P.codes + row * (UPS * kUnitBytes), (uint32_t)nvalid * UPS * kUnitBytes, full);
-        bulk_g2s(s_dst, P.scales + row * 64, (uint32_t)nvalid * 64, full);
-        bulk_g2s(z_dst, P.zeros + row * 16, (uint32_t)nvalid * 16, full);
+        bulk_g2s(st + P.c_off, P.codes + row * (UPS * kUnitBytes), (uint32_t)nvalid * UPS * kUnitBytes, full);
+        bulk_g2s(st + s_off, P.scales + row * 64, (uint32_t)nvalid * 64, full);
+        bulk_g2s(st + z_off, P.zeros + row * 16, (uint32_t)nvalid * 16, full);
       };
       auto issue_x = [&](int i) {
         const int slot = i % stages;
@@ -135,7 +133,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
         const uint32_t st = base + slot * P.stage_bytes;
 #pragma unroll
         for (int u = 0; u < UPS; ++u)
-          tma_load_2d(st + u * MT * 1024, &tmX, (sg * UPS + u) * kUnitK, 0, bar_full + 8 * slot);
+          tma_load_2d(st + u * P.x_unit, &tmX, (sg * UPS + u) * kUnitK, 0, bar_full + 8 * slot);
       };
       // Fill the ring with weights first: they do not depend on the
       // preceding kernel.  X does, so its loads wait for that grid.
@@ -177,83 +175,177 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[j][m][e] = 0.f;
 
+    // B fragments of unit u: X rows mt*8 + gr, k = 16t .. 16t+15 (two 16-byte
+    // chunks of a 128-byte row).  Plain loads through a generic pointer into
+    // shared memory: the compiler may hoist them ahead of earlier MMAs; the
+    // barrier wait clobbers memory, so none moves before it.
+    auto load_x = [&](const uint8_t* stg, int u, uint4 (&xa)[MT], uint4 (&xb)[MT]) {
+      if constexpr (XP) {
+        // M plain rows: rows at or past M do not exist and read as zeros.
+        const int r = min(gr, P.M - 1);
+        const uint8_t* row = stg + u * P.x_unit + r * 128;
+        uint4 a = *reinterpret_cast<const uint4*>(row + 32 * t);
+        uint4 b = *reinterpret_cast<const uint4*>(row + 32 * t + 16);
+        if (gr >= P.M) {
+          a = make_uint4(0, 0, 0, 0);
+          b = make_uint4(0, 0, 0, 0);
+        }
+        xa[0] = a;
+        xb[0] = b;
+      } else {
+        // 8 MT rows, 128-byte swizzle (chunk c of row r at c ^ (r & 7)); rows
+        // at or past M were zero-filled by the copy.
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const uint8_t* row = stg + (u * MT + m) * 1024 + gr * 128;
+          xa[m] = *reinterpret_cast<const uint4*>(row + (((2 * t) ^ gr) << 4));
+          xb[m] = *reinterpret_cast<const uint4*>(row + (((2 * t + 1) ^ gr) << 4));
+        }
+      }
+    };
+
     int slot = 0;
     uint32_t ph = 0;
     for (int i = 0; i < nsg; ++i) {
       if (!mbar_wait(bar_full + 8 * slot, ph, abort_flag, &s_err_decode)) break;
-      const uint32_t st = base + slot * P.stage_bytes;
-      const uint32_t c_base = st + SH::X_BYTES;
-      const uint32_t s_base = c_base + SH::C_BYTES;
-      const uint32_t z_base = s_base + SH::S_BYTES;
+      const uint8_t* stg = smem + (size_t)slot * P.stage_bytes;
+      const uint8_t* cg = stg + P.c_off;
+      const uint8_t* sgp = stg + s_off;
+      const uint8_t* zg = stg + z_off;
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
         float s_lo[WN], s_hi[WN];
-        uint32_t zz[WN], zf[WN];
+        uint32_t zlo[WN], zhi[WN];
 #pragma unroll
         for (int j = 0; j < WN; ++j) {
           const int jj = warp * WN + j;
-          const uint32_t sp = lds32(s_base + jj * 64 + gi * 32 + gr * 4);
+          const uint32_t sp = *reinterpret_cast<const uint32_t*>(sgp + jj * 64 + gi * 32 + gr * 4);
           s_lo[j] = __half2float(__ushort_as_half((unsigned short)(sp & 0xFFFFu)));
           s_hi[j] = __half2float(__ushort_as_half((unsigned short)(sp >> 16)));
-          const uint32_t zw = lds32(z_base + jj * 16 + gi * 8 + (gr & ~3));
-          const uint32_t zb = (zw >> (8 * (gr & 3))) & 0xFFu;
-          zz[j] = zero_pair_lo(zb & 15u);
-          zf[j] = zero_pair_hi(zb >> 4);
+          const uint32_t zb = zg[jj * 16 + gi * 8 + gr];
+          zlo[j] = zb & 15u;
+          zhi[j] = zb >> 4;
         }
-        float tmp[WN][MT][4];
+        if constexpr (kRaw) {
+          // d_lo = sum x (1024 + q), d_hi = sum x (1024 + 16 q) per row pair and
+          // xs = sum x (all-ones fragment), so
+          // sum x (q - z) = d_lo - (1024 + z) xs = (d_hi - (1024 + 16 z) xs) / 16.
+          float zc_lo[WN], zc_hi[WN];
 #pragma unroll
-        for (int j = 0; j < WN; ++j)
-#pragma unroll
-          for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) tmp[j][m][e] = 0.f;
-#pragma unroll
-        for (int uu = 0; uu < UPG; ++uu) {
-          const int u = gi * UPG + uu;
-          // B fragments: X rows mt*8+gr, k = 16t .. 16t+15 of this unit (two
-          // 16-byte chunks of a 128-byte swizzled row).  Rows at or past M
-          // are zeros in shared memory; they are not loaded at all.
-          uint4 xa[MT], xb[MT];
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            if (m * 8 + gr < P.M) {
-              const uint32_t row = st + (u * MT + m) * 1024 + gr * 128;
-              xa[m] = lds128(row + (((2 * t) ^ gr) << 4));
-              xb[m] = lds128(row + (((2 * t + 1) ^ gr) << 4));
-            } else {
-              xa[m] = make_uint4(0, 0, 0, 0);
-              xb[m] = make_uint4(0, 0, 0, 0);
-            }
+          for (int j = 0; j < WN; ++j) {
+            zc_lo[j] = (float)(1024u + zlo[j]);
+            zc_hi[j] = (float)(1024u + 16u * zhi[j]);
+            s_hi[j] *= 0.0625f;
           }
-          uint4 cw[WN];
+          constexpr uint32_t kOne2 = 0x3C003C00u;  // 1.0 in both halves
+          const uint32_t ones[4] = {kOne2, kOne2, kOne2, kOne2};
+          float d[WN][MT][4], xs[MT][4];
 #pragma unroll
-          for (int j = 0; j < WN; ++j)
-            cw[j] = lds128(c_base + ((warp * WN + j) * UPS + u) * kUnitBytes + lane * 16);
+          for (int uu = 0; uu < UPG; ++uu) {
+            const int u = gi * UPG + uu;
+            uint4 xa[MT], xb[MT];
+            load_x(stg, u, xa, xb);
+            uint4 cw[WN];
 #pragma unroll
-          for (int stp = 0; stp < 4; ++stp) {
+            for (int j = 0; j < WN; ++j)
+              cw[j] = *reinterpret_cast<const uint4*>(cg + ((warp * WN + j) * UPS + u) * kUnitBytes + lane * 16);
 #pragma unroll
-            for (int j = 0; j < WN; ++j) {
-              const uint32_t w = stp == 0 ? cw[j].x : stp == 1 ? cw[j].y : stp == 2 ? cw[j].z : cw[j].w;
-              uint32_t a[4];
-              dequant_word(w, zz[j], zf[j], a);
+            for (int stp = 0; stp < 4; ++stp) {
+              const bool first = (uu == 0 && stp == 0);
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
                 const uint32_t b0 = stp == 0 ? xa[m].x : stp == 1 ? xa[m].z : stp == 2 ? xb[m].x : xb[m].z;
                 const uint32_t b1 = stp == 0 ? xa[m].y : stp == 1 ? xa[m].w : stp == 2 ? xb[m].y : xb[m].w;
-                mma_16816(tmp[j][m], a, b0, b1);
+                if (first) {
+                  mma_16816_zc(xs[m], ones, b0, b1);
+                } else {
+                  mma_16816(xs[m], ones, b0, b1);
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < WN; ++j) {
+                const uint32_t w = stp == 0 ? cw[j].x : stp == 1 ? cw[j].y : stp == 2 ? cw[j].z : cw[j].w;
+                uint32_t a[4];
+                raw_word(w, a);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                  const uint32_t b0 = stp == 0 ? xa[m].x : stp == 1 ? xa[m].z : stp == 2 ? xb[m].x : xb[m].z;
+                  const uint32_t b1 = stp == 0 ? xa[m].y : stp == 1 ? xa[m].w : stp == 2 ? xb[m].y : xb[m].w;
+                  if (first) {
+                    mma_16816_zc(d[j][m], a, b0, b1);
+                  } else {
+                    mma_16816(d[j][m], a, b0, b1);
+                  }
+                }
               }
             }
           }
-        }
 #pragma unroll
-        for (int j = 0; j < WN; ++j)
+          for (int j = 0; j < WN; ++j)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            acc[j][m][0] = fmaf(s_lo[j], tmp[j][m][0], acc[j][m][0]);
-            acc[j][m][1] = fmaf(s_lo[j], tmp[j][m][1], acc[j][m][1]);
-            acc[j][m][2] = fmaf(s_hi[j], tmp[j][m][2], acc[j][m][2]);
-            acc[j][m][3] = fmaf(s_hi[j], tmp[j][m][3], acc[j][m][3]);
+            for (int m = 0; m < MT; ++m) {
+              acc[j][m][0] = fmaf(s_lo[j], fmaf(-zc_lo[j], xs[m][0], d[j][m][0]), acc[j][m][0]);
+              acc[j][m][1] = fmaf(s_lo[j], fmaf(-zc_lo[j], xs[m][1], d[j][m][1]), acc[j][m][1]);
+              acc[j][m][2] = fmaf(s_hi[j], fmaf(-zc_hi[j], xs[m][0], d[j][m][2]), acc[j][m][2]);
+              acc[j][m][3] = fmaf(s_hi[j], fmaf(-zc_hi[j], xs[m][1], d[j][m][3]), acc[j][m][3]);
+            }
+        } else {
+          uint32_t zz[WN], zf[WN];
+#pragma unroll
+          for (int j = 0; j < WN; ++j) {
+            zz[j] = zero_pair_lo(zlo[j]);
+            zf[j] = zero_pair_hi(zhi[j]);
           }
+          float tmp[NACC][WN][MT][4];
+#pragma unroll
+          for (int uu = 0; uu < UPG; ++uu) {
+            const int u = gi * UPG + uu;
+            uint4 xa[MT], xb[MT];
+            load_x(stg, u, xa, xb);
+            uint4 cw[WN];
+#pragma unroll
+            for (int j = 0; j < WN; ++j)
+              cw[j] = *reinterpret_cast<const uint4*>(cg + ((warp * WN + j) * UPS + u) * kUnitBytes + lane * 16);
+#pragma unroll
+            for (int stp = 0; stp < 4; ++stp) {
+              const int idx = uu * 4 + stp;
+              const int c = idx % NACC;
+              const bool first = idx < NACC;
+#pragma unroll
+              for (int j = 0; j < WN; ++j) {
+                const uint32_t w = stp == 0 ? cw[j].x : stp == 1 ? cw[j].y : stp == 2 ? cw[j].z : cw[j].w;
+                uint32_t a[4];
+                dequant_word(w, zz[j], zf[j], a);
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                  const uint32_t b0 = stp == 0 ? xa[m].x : stp == 1 ? xa[m].z : stp == 2 ? xb[m].x : xb[m].z;
+                  const uint32_t b1 = stp == 0 ? xa[m].y : stp == 1 ? xa[m].w : stp == 2 ? xb[m].y : xb[m].w;
+                  if (first) {
+                    mma_16816_zc(tmp[c][j][m], a, b0, b1);
+                  } else {
+                    mma_16816(tmp[c][j][m], a, b0, b1);
+                  }
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < WN; ++j)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              float v[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[e] = tmp[0][j][m][e];
+#pragma unroll
+                for (int c = 1; c < NACC; ++c) v[e] += tmp[c][j][m][e];
+              }
+              acc[j][m][0] = fmaf(s_lo[j], v[0], acc[j][m][0]);
+              acc[j][m][1] = fmaf(s_lo[j], v[1], acc[j][m][1]);
+              acc[j][m][2] = fmaf(s_hi[j], v[2], acc[j][m][2]);
+              acc[j][m][3] = fmaf(s_hi[j], v[3], acc[j][m][3]);
+            }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
@@ -265,7 +357,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
 
     // Partial tile -> the owner of each column slice: red[rank][m][col] in
     // the owner's shared memory (its own when S == 1).
-    const int span = SH::CNN / S;
+    const int span = CNN / S;
     const uint32_t my_rank = S > 1 ? cluster_ctarank() : 0u;
     const uint32_t red_s = smem_u32(red);
     if (S > 1) cluster_wait();
@@ -297,7 +389,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
     __syncthreads();
   }
   grid_dependency_wait();  // Y may still be read by the preceding grid
-  const int span = SH::CNN / S;
+  const int span = CNN / S;
   const uint32_t my_rank = S > 1 ? cluster_ctarank() : 0u;
   const int half_span = span >> 1;
   const int items = P.M * half_span;
@@ -336,7 +428,8 @@ cudaError_t decode_error_bits(uint32_t* bits, bool clear) {
 
 namespace {
 
-constexpr uint32_t kSmemBudget = 113 * 1024;  // two CTAs per SM at least
+constexpr uint32_t kSmemPerSM = 228 * 1024;
+constexpr uint32_t kSmemPerCta = 227 * 1024;
 
 int mt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
@@ -350,19 +443,44 @@ bool tile_shape(int tile_n, int MT, int* WN, int* NW) {
   return false;
 }
 
-uint32_t stage_bytes_rt(int MT, int CN, int UPS) {
-  const uint32_t raw = UPS * MT * 1024 + CN * UPS * kUnitBytes + CN * 64 + CN * 16;
-  return (raw + 1023) & ~1023u;
+struct Geometry {
+  bool xp;             // X as M plain rows
+  uint32_t x_unit;     // bytes of X per unit
+  uint32_t c_off;      // codes offset in a stage
+  uint32_t stage;      // bytes per stage
+  uint32_t red;        // reduction buffer
+  uint32_t codes;      // code bytes per stage
+};
+
+Geometry geometry(int M, int MT, int CN, int UPS) {
+  Geometry g;
+  g.xp = MT == 1 && M < 8;
+  g.x_unit = g.xp ? (uint32_t)M * 128u : (uint32_t)MT * 1024u;
+  g.c_off = UPS * g.x_unit;  // a multiple of 128 (plain) or 1024 (swizzled)
+  g.codes = (uint32_t)CN * UPS * kUnitBytes;
+  g.stage = (g.c_off + g.codes + CN * 80u + 1023u) & ~1023u;
+  g.red = (uint32_t)MT * 8 * CN * 16 * 4;
+  return g;
 }
 
-uint32_t red_bytes_rt(int MT, int CN) { return MT * 8 * CN * 16 * 4; }
+uint32_t smem_bytes(const Geometry& g, int stages) {
+  const uint32_t bar_off = (g.stage * stages + g.red + 15u) & ~15u;
+  return bar_off + 16 * stages + 16 + 1024;  // + alignment slack
+}
 
-template <int MT, int WN, int NW, int UPS>
+// Largest stage count that fits `budget` bytes of shared memory.
+int fit_stages(const Geometry& g, uint32_t budget) {
+  int s = 8;
+  while (s >= 2 && smem_bytes(g, s) > budget) --s;
+  return s;
+}
+
+template <int MT, int WN, int NW, int UPS, bool XP>
 tm_status launch_t(const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem, cudaStream_t stream) {
-  auto kern = decode_kernel<MT, WN, NW, UPS>;
+  auto kern = decode_kernel<MT, WN, NW, UPS, XP>;
   static bool attr_done = false;  // per instantiation, per process
   if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemPerCta) != cudaSuccess)
       return TM_ERR_CUDA;
     attr_done = true;
   }
@@ -390,22 +508,40 @@ tm_status launch_t(const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_
   return e == cudaSuccess ? TM_OK : TM_ERR_CUDA;
 }
 
-template <int MT, int WN, int NW>
+template <int MT, int WN, int NW, bool XP>
 tm_status launch_u(int UPS, const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem,
                    cudaStream_t stream) {
-  return UPS == 4 ? launch_t<MT, WN, NW, 4>(tmX, P, S, smem, stream)
-                  : launch_t<MT, WN, NW, 2>(tmX, P, S, smem, stream);
+  return UPS == 4 ? launch_t<MT, WN, NW, 4, XP>(tmX, P, S, smem, stream)
+                  : launch_t<MT, WN, NW, 2, XP>(tmX, P, S, smem, stream);
 }
 
-template <int MT>
+template <int MT, bool XP>
 tm_status launch_m(int tile_n, int UPS, const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem,
                    cudaStream_t stream) {
-  if (tile_n == 64) return launch_u<MT, 1, 4>(UPS, tmX, P, S, smem, stream);
-  if (tile_n == 128) return launch_u<MT, 1, 8>(UPS, tmX, P, S, smem, stream);
+  if (tile_n == 64) return launch_u<MT, 1, 4, XP>(UPS, tmX, P, S, smem, stream);
+  if (tile_n == 128) return launch_u<MT, 1, 8, XP>(UPS, tmX, P, S, smem, stream);
   if constexpr (MT <= 4) {
-    if (tile_n == 256) return launch_u<MT, 2, 8>(UPS, tmX, P, S, smem, stream);
+    if (tile_n == 256) return launch_u<MT, 2, 8, XP>(UPS, tmX, P, S, smem, stream);
   }
   return TM_ERR_UNSUPPORTED;
+}
+
+// Rough time model of one launch, used only to rank launch shapes:
+//   * memory: the weights at the HBM rate;
+//   * latency: a CTA can have `stages` stages in flight; each round trip
+//     under load takes about kLoadedLatencyUs, so a CTA with `per_cta`
+//     stages needs per_cta / stages round trips;
+//   * a fixed cost per launch plus a cost per cluster barrier level.
+double model_us(double weight_bytes, int per_cta, int stages, int S, int ctas, int sms) {
+  constexpr double kHbmBytesPerUs = 6.5e6;
+  constexpr double kLoadedLatencyUs = 2.5;
+  const double t_mem = weight_bytes / kHbmBytesPerUs;
+  const double t_lat = (double)per_cta / stages * kLoadedLatencyUs;
+  const double fill = ctas >= sms ? 1.0 : (double)ctas / sms;  // idle SMs stream nothing
+  double t = std::max(t_mem / std::min(1.0, fill * 1.5), t_lat);
+  int lv = 0;
+  for (int s = S; s > 1; s >>= 1) ++lv;
+  return t + 1.0 + 0.35 * lv;
 }
 
 }  // namespace
@@ -413,33 +549,47 @@ tm_status launch_m(int tile_n, int UPS, const CUtensorMap& tmX, const DecodePara
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out) {
   const Layout& L = p->L;
   const int MT = mt_for(M);
-  int tile_n = in && in->tile_n ? in->tile_n : 128;
-  int WN = 0, NW = 0;
-  if (tile_n != 64 && tile_n != 128 && tile_n != 256) return TM_ERR_INVALID_ARG;
-  if (!tile_shape(tile_n, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
-  const int CN = NW * WN;
-  const int NB = (L.NT + CN - 1) / CN;
-  int S = in && in->split_k ? in->split_k : 0;
-  if (S == 0) {
-    const int target = 2 * num_sms(p->device);
-    S = 1;
-    while (S < 8 && NB * S < target && 2 * S <= L.NSG) S *= 2;
+  const int sms = num_sms(p->device);
+  const int want_tile = in ? in->tile_n : 0;
+  const int want_S = in ? in->split_k : 0;
+  const int want_stages = in ? in->stages : 0;
+  if (want_tile && want_tile != 64 && want_tile != 128 && want_tile != 256) return TM_ERR_INVALID_ARG;
+  if (want_S && want_S != 1 && want_S != 2 && want_S != 4 && want_S != 8) return TM_ERR_INVALID_ARG;
+  if (want_stages && (want_stages < 2 || want_stages > 8)) return TM_ERR_INVALID_ARG;
+  double best = 1e30;
+  tm_gemm_config pick = {0, 0, 0, 0};
+  const int tiles[3] = {64, 128, 256};
+  const int splits[4] = {1, 2, 4, 8};
+  for (int tile : tiles) {
+    if (want_tile && tile != want_tile) continue;
+    int WN = 0, NW = 0;
+    if (!tile_shape(tile, MT, &WN, &NW)) continue;
+    const int CN = WN * NW;
+    const int NB = (L.NT + CN - 1) / CN;
+    const Geometry g = geometry(M, MT, CN, L.UPS);
+    for (int S : splits) {
+      if (want_S && S != want_S) continue;
+      if (!want_S && S > 1 && S > L.NSG) continue;
+      const int ctas = NB * S;
+      const int per_cta = (L.NSG + S - 1) / S;
+      const int per_sm = (ctas + sms - 1) / sms;  // CTAs an SM holds at once for a single wave
+      uint32_t budget = kSmemPerCta;
+      if (per_sm > 1) budget = std::min(budget, kSmemPerSM / (uint32_t)std::min(per_sm, 8) - 1024u);
+      int stages = want_stages ? want_stages : std::min(fit_stages(g, budget), std::max(2, per_cta));
+      if (stages < 2 || smem_bytes(g, stages) > kSmemPerCta) continue;
+      const double t = model_us((double)ctas * per_cta * g.codes, per_cta, stages, S, ctas, sms) *
+                       (per_sm > 4 ? 1.0 + 0.1 * (per_sm - 4) : 1.0);
+      if (t < best) {
+        best = t;
+        pick.path = 1;
+        pick.split_k = S;
+        pick.tile_n = tile;
+        pick.stages = stages;
+      }
+    }
   }
-  if (S != 1 && S != 2 && S != 4 && S != 8) return TM_ERR_INVALID_ARG;
-  const uint32_t sb = stage_bytes_rt(MT, CN, L.UPS);
-  const int per_cta = (L.NSG + S - 1) / S;
-  int stages = in && in->stages ? in->stages : 0;
-  if (stages == 0) {
-    const uint32_t fixed = red_bytes_rt(MT, CN) + 1024 + 256;
-    stages = (int)((kSmemBudget - fixed) / sb);
-    stages = std::max(2, std::min(stages, 4));
-    stages = std::min(stages, std::max(2, per_cta));
-  }
-  if (stages < 2 || stages > 8) return TM_ERR_INVALID_ARG;
-  out->path = 1;
-  out->split_k = S;
-  out->tile_n = tile_n;
-  out->stages = stages;
+  if (pick.path == 0) return TM_ERR_UNSUPPORTED;
+  *out = pick;
   return TM_OK;
 }
 
@@ -451,19 +601,21 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   if (!tile_shape(c.tile_n, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
   const int CN = WN * NW;
   const int S = c.split_k;
-  // X as a 2-D tensor {K, M}: box = 64 k x (8 MT) rows, 128-byte swizzle;
-  // rows beyond M and columns beyond K read as zeros.
+  const Geometry g = geometry(M, MT, CN, L.UPS);
+  // X as a 2-D tensor {K, M}: box = 64 k x rows; rows beyond M and columns
+  // beyond K read as zeros.  8 MT rows with a 128-byte swizzle, or exactly M
+  // plain rows when M < 8.
   CUtensorMap tmX;
   {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return TM_ERR_CUDA;
     cuuint64_t dims[2] = {(cuuint64_t)L.K, (cuuint64_t)M};
     cuuint64_t strides[1] = {(cuuint64_t)L.K * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)(8 * MT)};
+    cuuint32_t box[2] = {64, (cuuint32_t)(g.xp ? M : 8 * MT)};
     cuuint32_t es[2] = {1, 1};
     if (fn(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(X), dims, strides, box, es,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+           CU_TENSOR_MAP_INTERLEAVE_NONE, g.xp ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TM_ERR_CUDA;
   }
   DecodeParams P;
@@ -477,17 +629,22 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   P.nsg_total = L.NSG;
   P.sg_per_cta = (P.nsg_total + S - 1) / S;
   P.stages = c.stages;
-  P.stage_bytes = stage_bytes_rt(MT, CN, L.UPS);
-  P.r_off = P.stage_bytes * c.stages;
-  P.bar_off = (P.r_off + red_bytes_rt(MT, CN) + 15) & ~15u;
-  const uint32_t smem = P.bar_off + 16 * c.stages + 16 + 1024;  // + alignment slack
-  if (smem > 227 * 1024) return TM_ERR_UNSUPPORTED;
+  P.x_unit = g.x_unit;
+  P.c_off = g.c_off;
+  P.stage_bytes = g.stage;
+  P.r_off = g.stage * c.stages;
+  P.bar_off = (P.r_off + g.red + 15u) & ~15u;
+  const uint32_t smem = smem_bytes(g, c.stages);
+  if (smem > kSmemPerCta) return TM_ERR_UNSUPPORTED;
   tm_status st;
   switch (MT) {
-    case 1: st = launch_m<1>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
-    case 2: st = launch_m<2>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
-    case 4: st = launch_m<4>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
-    case 8: st = launch_m<8>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
+    case 1:
+      st = g.xp ? launch_m<1, true>(c.tile_n, L.UPS, tmX, P, S, smem, stream)
+                : launch_m<1, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream);
+      break;
+    case 2: st = launch_m<2, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
+    case 4: st = launch_m<4, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
+    case 8: st = launch_m<8, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
     default: return TM_ERR_UNSUPPORTED;
   }
   if (st == TM_OK) set_launch_count(1);

@@ -280,20 +280,44 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zz_lo, uint32_
   out[3] = hfma2_u32(r3, kSixteenth, zf_hi);
 }
 
+// The raw form: the four A-fragment registers of a word without the zero
+// point, 5 instructions per 8 weights.
+//   out[0] = 1024 + q (row gr  , k, k+1)     out[1] = 1024 + 16 q (row gr+8, k, k+1)
+//   out[2] = 1024 + q (row gr  , k+2, k+3)   out[3] = 1024 + 16 q (row gr+8, k+2, k+3)
+// A product with these sums x (1024 + q) (resp. x (1024 + 16 q)); the zero
+// point and the offset are removed once per group with the sum of x.
+__device__ __forceinline__ void raw_word(uint32_t w, uint32_t out[4]) {
+  constexpr uint32_t kMagic = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  out[0] = lop3<0xEA>(w, 0x000F000Fu, kMagic);
+  out[1] = lop3<0xEA>(w, 0x00F000F0u, kMagic);
+  out[2] = lop3<0xEA>(w8, 0x000F000Fu, kMagic);
+  out[3] = lop3<0xEA>(w8, 0x00F000F0u, kMagic);
+}
+
 // (1024 + z) in both halves of a word.
 __device__ __forceinline__ uint32_t zero_pair_lo(uint32_t z) {
   const uint32_t h = 0x6400u | z;
   return h | (h << 16);
 }
-// -(64 + z) in both halves (exact: 64..79 are integers in fp16).
+// -(64 + z) in both halves: 64 + z (z < 16) is 2^6 (1 + z/64), i.e. the fp16
+// pattern 0x5400 + 16 z; the sign bit makes it 0xD400 + 16 z.
 __device__ __forceinline__ uint32_t zero_pair_hi(uint32_t z) {
-  const __half h = __float2half_rn(-(64.0f + (float)z));
-  const uint32_t b = __half_as_ushort(h);
+  const uint32_t b = 0xD400u + (z << 4);
   return b | (b << 16);
 }
 
+// d = a . b with a zero accumulator (no register moves to clear d).
+__device__ __forceinline__ void mma_16816_zc(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Pure register operation (not volatile): the compiler may schedule it freely.
 __device__ __forceinline__ void mma_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
