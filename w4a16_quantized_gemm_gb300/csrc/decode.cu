@@ -47,6 +47,7 @@ struct DecodeParams {
   int sg_per_cta;  // pairs of groups per CTA of a cluster
   int stages;
   uint32_t x_unit;       // bytes of X per 64-k unit in a stage
+  uint32_t x_box;        // bytes one X copy delivers per unit
   uint32_t c_off;        // offset of the codes in a stage
   uint32_t stage_bytes;  // bytes per stage (1024-aligned)
   uint32_t r_off;        // offset of the reduction buffer
@@ -66,7 +67,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
 
 // MT: 8-row tiles of X (M <= 8 MT); WN: n-tiles per consumer warp; NW:
 // consumer warps; UPS: 64-k units per stage (2g/64); XP: X stored as M plain
-// rows (M < 8) instead of 8 MT swizzled rows.
+// rows and one zero row (M < 8) instead of 8 MT swizzled rows.
 template <int MT, int WN, int NW, int UPS, bool XP>
 __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                const DecodeParams P) {
@@ -105,6 +106,15 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
     fence_mbar_init();
     launch_dependents();
   }
+  if constexpr (XP) {
+    // The zero row after the M rows of X in every unit slot: the copies never
+    // write it, so it stays zero for the whole kernel.
+    for (int i = threadIdx.x; i < stages * UPS * 8; i += blockDim.x) {
+      const int s8 = i & 7, su = i >> 3;
+      uint8_t* z = smem + (size_t)(su / UPS) * P.stage_bytes + (su % UPS) * P.x_unit + P.M * 128 + s8 * 16;
+      *reinterpret_cast<uint4*>(z) = make_uint4(0, 0, 0, 0);
+    }
+  }
   __syncthreads();
   // Every CTA of the cluster must be running before any CTA stores into its
   // shared memory: arrive now, wait right before the first remote store.
@@ -115,7 +125,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
     if (lane == 0) {
       prefetch_tmap(&tmX);
       const int nvalid = min(CN, P.NT - nt0);
-      const uint32_t tx = UPS * P.x_unit + (uint32_t)nvalid * (UPS * kUnitBytes + 64 + 16);
+      const uint32_t tx = UPS * P.x_box + (uint32_t)nvalid * (UPS * kUnitBytes + 64 + 16);
       auto issue_weights = [&](int i) {
         const int slot = i % stages;
         const int sg = sg_begin + i;
@@ -181,17 +191,11 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
     // barrier wait clobbers memory, so none moves before it.
     auto load_x = [&](const uint8_t* stg, int u, uint4 (&xa)[MT], uint4 (&xb)[MT]) {
       if constexpr (XP) {
-        // M plain rows: rows at or past M do not exist and read as zeros.
-        const int r = min(gr, P.M - 1);
+        // M plain rows and, after them, a row of zeros that lanes past M read.
+        const int r = min(gr, P.M);
         const uint8_t* row = stg + u * P.x_unit + r * 128;
-        uint4 a = *reinterpret_cast<const uint4*>(row + 32 * t);
-        uint4 b = *reinterpret_cast<const uint4*>(row + 32 * t + 16);
-        if (gr >= P.M) {
-          a = make_uint4(0, 0, 0, 0);
-          b = make_uint4(0, 0, 0, 0);
-        }
-        xa[0] = a;
-        xb[0] = b;
+        xa[0] = *reinterpret_cast<const uint4*>(row + 32 * t);
+        xb[0] = *reinterpret_cast<const uint4*>(row + 32 * t + 16);
       } else {
         // 8 MT rows, 128-byte swizzle (chunk c of row r at c ^ (r & 7)); rows
         // at or past M were zero-filled by the copy.
@@ -428,7 +432,6 @@ cudaError_t decode_error_bits(uint32_t* bits, bool clear) {
 
 namespace {
 
-constexpr uint32_t kSmemPerSM = 228 * 1024;
 constexpr uint32_t kSmemPerCta = 227 * 1024;
 
 int mt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
@@ -455,7 +458,7 @@ struct Geometry {
 Geometry geometry(int M, int MT, int CN, int UPS) {
   Geometry g;
   g.xp = MT == 1 && M < 8;
-  g.x_unit = g.xp ? (uint32_t)M * 128u : (uint32_t)MT * 1024u;
+  g.x_unit = g.xp ? (uint32_t)(M + 1) * 128u : (uint32_t)MT * 1024u;  // plain: M rows + a zero row
   g.c_off = UPS * g.x_unit;  // a multiple of 128 (plain) or 1024 (swizzled)
   g.codes = (uint32_t)CN * UPS * kUnitBytes;
   g.stage = (g.c_off + g.codes + CN * 80u + 1023u) & ~1023u;
@@ -526,40 +529,28 @@ tm_status launch_m(int tile_n, int UPS, const CUtensorMap& tmX, const DecodePara
   return TM_ERR_UNSUPPORTED;
 }
 
-// Rough time model of one launch, used only to rank launch shapes:
-//   * memory: the weights at the HBM rate;
-//   * latency: a CTA can have `stages` stages in flight; each round trip
-//     under load takes about kLoadedLatencyUs, so a CTA with `per_cta`
-//     stages needs per_cta / stages round trips;
-//   * a fixed cost per launch plus a cost per cluster barrier level.
-double model_us(double weight_bytes, int per_cta, int stages, int S, int ctas, int sms) {
-  constexpr double kHbmBytesPerUs = 6.5e6;
-  constexpr double kLoadedLatencyUs = 2.5;
-  const double t_mem = weight_bytes / kHbmBytesPerUs;
-  const double t_lat = (double)per_cta / stages * kLoadedLatencyUs;
-  const double fill = ctas >= sms ? 1.0 : (double)ctas / sms;  // idle SMs stream nothing
-  double t = std::max(t_mem / std::min(1.0, fill * 1.5), t_lat);
-  int lv = 0;
-  for (int s = S; s > 1; s >>= 1) ++lv;
-  return t + 1.0 + 0.35 * lv;
-}
-
 }  // namespace
 
+// Launch shape.  Measured on GB300 over the Llama-3 8B/70B decode shapes: the
+// fastest shapes keep many small CTAs resident (256 or more per launch)
+// with shallow rings -- more consumer warps per SM beat deeper prefetch --
+// so the rule is: 128 columns per CTA (else 64, else 256), the smallest
+// cluster split giving at least 256 CTAs, 4 stages for M <= 16 and 2 above.
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out) {
   const Layout& L = p->L;
   const int MT = mt_for(M);
-  const int sms = num_sms(p->device);
   const int want_tile = in ? in->tile_n : 0;
   const int want_S = in ? in->split_k : 0;
   const int want_stages = in ? in->stages : 0;
   if (want_tile && want_tile != 64 && want_tile != 128 && want_tile != 256) return TM_ERR_INVALID_ARG;
   if (want_S && want_S != 1 && want_S != 2 && want_S != 4 && want_S != 8) return TM_ERR_INVALID_ARG;
   if (want_stages && (want_stages < 2 || want_stages > 8)) return TM_ERR_INVALID_ARG;
-  double best = 1e30;
-  tm_gemm_config pick = {0, 0, 0, 0};
-  const int tiles[3] = {64, 128, 256};
+  constexpr int kMinCtas = 256;
+  const int tiles[3] = {128, 64, 256};
   const int splits[4] = {1, 2, 4, 8};
+  tm_gemm_config pick = {0, 0, 0, 0};
+  tm_gemm_config fallback = {0, 0, 0, 0};  // the shape with the most CTAs
+  int fallback_ctas = 0;
   for (int tile : tiles) {
     if (want_tile && tile != want_tile) continue;
     int WN = 0, NW = 0;
@@ -569,25 +560,24 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
     const Geometry g = geometry(M, MT, CN, L.UPS);
     for (int S : splits) {
       if (want_S && S != want_S) continue;
-      if (!want_S && S > 1 && S > L.NSG) continue;
-      const int ctas = NB * S;
+      if (!want_S && S > 1 && S > L.NSG) break;
       const int per_cta = (L.NSG + S - 1) / S;
-      const int per_sm = (ctas + sms - 1) / sms;  // CTAs an SM holds at once for a single wave
-      uint32_t budget = kSmemPerCta;
-      if (per_sm > 1) budget = std::min(budget, kSmemPerSM / (uint32_t)std::min(per_sm, 8) - 1024u);
-      int stages = want_stages ? want_stages : std::min(fit_stages(g, budget), std::max(2, per_cta));
+      int stages = want_stages ? want_stages : std::min(MT <= 2 ? 4 : 2, std::max(2, per_cta));
+      if (!want_stages) stages = std::min(stages, std::max(2, fit_stages(g, kSmemPerCta)));
       if (stages < 2 || smem_bytes(g, stages) > kSmemPerCta) continue;
-      const double t = model_us((double)ctas * per_cta * g.codes, per_cta, stages, S, ctas, sms) *
-                       (per_sm > 4 ? 1.0 + 0.1 * (per_sm - 4) : 1.0);
-      if (t < best) {
-        best = t;
-        pick.path = 1;
-        pick.split_k = S;
-        pick.tile_n = tile;
-        pick.stages = stages;
+      const tm_gemm_config c = {1, S, tile, stages};
+      if (NB * S > fallback_ctas) {
+        fallback = c;
+        fallback_ctas = NB * S;
+      }
+      if (NB * S >= kMinCtas || want_S) {
+        pick = c;
+        break;
       }
     }
+    if (pick.path) break;
   }
+  if (pick.path == 0) pick = fallback;
   if (pick.path == 0) return TM_ERR_UNSUPPORTED;
   *out = pick;
   return TM_OK;
@@ -630,6 +620,7 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   P.sg_per_cta = (P.nsg_total + S - 1) / S;
   P.stages = c.stages;
   P.x_unit = g.x_unit;
+  P.x_box = g.xp ? (uint32_t)M * 128u : (uint32_t)MT * 1024u;
   P.c_off = g.c_off;
   P.stage_bytes = g.stage;
   P.r_off = g.stage * c.stages;
