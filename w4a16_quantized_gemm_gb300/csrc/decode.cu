@@ -74,7 +74,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
   constexpr int CN = NW * WN;    // n-tiles per CTA
   constexpr int CNN = CN * 16;   // columns per CTA
   constexpr int UPG = UPS / 2;   // units (of 64 k) per group
-  constexpr int NACC = MT == 1 ? 2 : 1;  // independent accumulator chains
+  constexpr int NACC = 1;  // accumulator chains per tile (more measured slower)
   // Raw-code products pay off when the all-ones product is shared by several tiles.
   constexpr bool kRaw = WN >= 2 && MT < 4 * WN;
   extern __shared__ uint8_t smem_raw[];
