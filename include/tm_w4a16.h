@@ -52,6 +52,7 @@ typedef struct {
   int split_k; /* 0 auto, else number of CTAs (a thread-block cluster, 1..8) sharing one output tile along K */
   int tile_n;  /* 0 auto, else output columns per CTA (decode 64/128/256, prefill 128/256) */
   int stages;  /* 0 auto, else pipeline depth in shared memory (2..8) */
+  int warp_n;  /* decode only: 0 auto, else 16-column tiles per consumer warp (1, 2 or 4) */
 } tm_gemm_config;
 
 /* Human-readable name of a status (static string, never NULL). */

@@ -436,14 +436,21 @@ constexpr uint32_t kSmemPerCta = 227 * 1024;
 
 int mt_for(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
-// tile_n -> (WN, NW)
-bool tile_shape(int tile_n, int MT, int* WN, int* NW) {
-  switch (tile_n) {
-    case 64: *WN = 1; *NW = 4; return true;
-    case 128: *WN = 1; *NW = 8; return true;
-    case 256: *WN = 2; *NW = 8; return MT <= 4;
-  }
-  return false;
+// (tile_n, warp_n) -> (WN n-tiles per warp, NW consumer warps).  Served:
+// WN 1 with 4 or 8 warps, WN 2 with 4 or 8 warps (M <= 32), WN 4 with 2 or
+// 4 warps (M <= 16).
+bool tile_shape(int tile_n, int warp_n, int MT, int* WN, int* NW) {
+  if (warp_n != 1 && warp_n != 2 && warp_n != 4) return false;
+  if (tile_n % (16 * warp_n)) return false;
+  const int nw = tile_n / (16 * warp_n);
+  bool ok = false;
+  if (warp_n == 1) ok = nw == 4 || nw == 8;
+  if (warp_n == 2) ok = (nw == 4 || nw == 8) && MT <= 4;
+  if (warp_n == 4) ok = (nw == 2 || nw == 4) && MT <= 2;
+  if (!ok) return false;
+  *WN = warp_n;
+  *NW = nw;
+  return true;
 }
 
 struct Geometry {
@@ -519,12 +526,17 @@ tm_status launch_u(int UPS, const CUtensorMap& tmX, const DecodeParams& P, int S
 }
 
 template <int MT, bool XP>
-tm_status launch_m(int tile_n, int UPS, const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem,
+tm_status launch_m(int WN, int NW, int UPS, const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem,
                    cudaStream_t stream) {
-  if (tile_n == 64) return launch_u<MT, 1, 4, XP>(UPS, tmX, P, S, smem, stream);
-  if (tile_n == 128) return launch_u<MT, 1, 8, XP>(UPS, tmX, P, S, smem, stream);
+  if (WN == 1 && NW == 4) return launch_u<MT, 1, 4, XP>(UPS, tmX, P, S, smem, stream);
+  if (WN == 1 && NW == 8) return launch_u<MT, 1, 8, XP>(UPS, tmX, P, S, smem, stream);
   if constexpr (MT <= 4) {
-    if (tile_n == 256) return launch_u<MT, 2, 8, XP>(UPS, tmX, P, S, smem, stream);
+    if (WN == 2 && NW == 4) return launch_u<MT, 2, 4, XP>(UPS, tmX, P, S, smem, stream);
+    if (WN == 2 && NW == 8) return launch_u<MT, 2, 8, XP>(UPS, tmX, P, S, smem, stream);
+  }
+  if constexpr (MT <= 2) {
+    if (WN == 4 && NW == 2) return launch_u<MT, 4, 2, XP>(UPS, tmX, P, S, smem, stream);
+    if (WN == 4 && NW == 4) return launch_u<MT, 4, 4, XP>(UPS, tmX, P, S, smem, stream);
   }
   return TM_ERR_UNSUPPORTED;
 }
@@ -542,19 +554,31 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
   const int want_tile = in ? in->tile_n : 0;
   const int want_S = in ? in->split_k : 0;
   const int want_stages = in ? in->stages : 0;
+  const int want_wn = in ? in->warp_n : 0;
   if (want_tile && want_tile != 64 && want_tile != 128 && want_tile != 256) return TM_ERR_INVALID_ARG;
   if (want_S && want_S != 1 && want_S != 2 && want_S != 4 && want_S != 8) return TM_ERR_INVALID_ARG;
   if (want_stages && (want_stages < 2 || want_stages > 8)) return TM_ERR_INVALID_ARG;
+  if (want_wn && want_wn != 1 && want_wn != 2 && want_wn != 4) return TM_ERR_INVALID_ARG;
   constexpr int kMinCtas = 256;
   const int tiles[3] = {128, 64, 256};
   const int splits[4] = {1, 2, 4, 8};
-  tm_gemm_config pick = {0, 0, 0, 0};
-  tm_gemm_config fallback = {0, 0, 0, 0};  // the shape with the most CTAs
+  tm_gemm_config pick = {0, 0, 0, 0, 0};
+  tm_gemm_config fallback = {0, 0, 0, 0, 0};  // the shape with the most CTAs
   int fallback_ctas = 0;
   for (int tile : tiles) {
     if (want_tile && tile != want_tile) continue;
-    int WN = 0, NW = 0;
-    if (!tile_shape(tile, MT, &WN, &NW)) continue;
+    // one 16-column tile per warp unless requested otherwise (measured fastest);
+    // a tile only served with more per warp takes the first that fits
+    int WN = 0, NW = 0, wn = 0;
+    const int wns[3] = {1, 2, 4};
+    for (int w : wns) {
+      if (want_wn && w != want_wn) continue;
+      if (tile_shape(tile, w, MT, &WN, &NW)) {
+        wn = w;
+        break;
+      }
+    }
+    if (!wn) continue;
     const int CN = WN * NW;
     const int NB = (L.NT + CN - 1) / CN;
     const Geometry g = geometry(M, MT, CN, L.UPS);
@@ -562,10 +586,10 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
       if (want_S && S != want_S) continue;
       if (!want_S && S > 1 && S > L.NSG) break;
       const int per_cta = (L.NSG + S - 1) / S;
-      int stages = want_stages ? want_stages : std::min(MT <= 2 ? 4 : 2, std::max(2, per_cta));
+      int stages = want_stages ? want_stages : std::min(MT <= 2 ? 3 : 2, std::max(2, per_cta));
       if (!want_stages) stages = std::min(stages, std::max(2, fit_stages(g, kSmemPerCta)));
       if (stages < 2 || smem_bytes(g, stages) > kSmemPerCta) continue;
-      const tm_gemm_config c = {1, S, tile, stages};
+      const tm_gemm_config c = {1, S, tile, stages, wn};
       if (NB * S > fallback_ctas) {
         fallback = c;
         fallback_ctas = NB * S;
@@ -588,7 +612,7 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   const Layout& L = p->L;
   const int MT = mt_for(M);
   int WN = 0, NW = 0;
-  if (!tile_shape(c.tile_n, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
+  if (!tile_shape(c.tile_n, c.warp_n, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
   const int CN = WN * NW;
   const int S = c.split_k;
   const Geometry g = geometry(M, MT, CN, L.UPS);
@@ -630,12 +654,12 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   tm_status st;
   switch (MT) {
     case 1:
-      st = g.xp ? launch_m<1, true>(c.tile_n, L.UPS, tmX, P, S, smem, stream)
-                : launch_m<1, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream);
+      st = g.xp ? launch_m<1, true>(WN, NW, L.UPS, tmX, P, S, smem, stream)
+                : launch_m<1, false>(WN, NW, L.UPS, tmX, P, S, smem, stream);
       break;
-    case 2: st = launch_m<2, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
-    case 4: st = launch_m<4, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
-    case 8: st = launch_m<8, false>(c.tile_n, L.UPS, tmX, P, S, smem, stream); break;
+    case 2: st = launch_m<2, false>(WN, NW, L.UPS, tmX, P, S, smem, stream); break;
+    case 4: st = launch_m<4, false>(WN, NW, L.UPS, tmX, P, S, smem, stream); break;
+    case 8: st = launch_m<8, false>(WN, NW, L.UPS, tmX, P, S, smem, stream); break;
     default: return TM_ERR_UNSUPPORTED;
   }
   if (st == TM_OK) set_launch_count(1);

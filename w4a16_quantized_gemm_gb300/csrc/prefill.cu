@@ -304,6 +304,7 @@ tm_status plan_prefill(const tm_packed* p, int M, const tm_gemm_config* in, tm_g
   out->split_k = S;
   out->tile_n = tile_n;
   out->stages = stages;
+  out->warp_n = 0;
   return TM_OK;
 }
 
