@@ -183,3 +183,18 @@ def test_one_launch_per_call():
 def test_no_device_errors_left():
     torch.cuda.synchronize()
     assert binding.device_error(clear=False) == 0
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("K", [256, 1024])
+def test_prefill_split_override(split, K):
+    """Split K over a cluster; with K = 256 and 8 CTAs some CTAs get no K block."""
+    err, _ = run_and_compare(200, K, 512, 128, config={"path": 2, "split_k": split})
+    assert err <= TOL, err
+
+
+def test_prefill_auto_split_small_m():
+    w = packed(4096, 4096, 128)
+    assert binding.plan(w, 128)["split_k"] > 1
+    err, _ = run_and_compare(128, 4096, 4096, 128)
+    assert err <= TOL, err
