@@ -41,6 +41,27 @@ int num_sms(int device) {
   return g_sms[device];
 }
 
+void sm_shared_memory(int device, int* per_sm, int* reserved_per_cta) {
+  static int cache[64][2];
+  if (device < 0 || device >= 64) {
+    *per_sm = 228 * 1024;
+    *reserved_per_cta = 1024;
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!cache[device][0]) {
+    int a = 0, b = 0;
+    if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess || a <= 0)
+      a = 228 * 1024;
+    if (cudaDeviceGetAttribute(&b, cudaDevAttrReservedSharedMemoryPerBlock, device) != cudaSuccess || b < 0)
+      b = 1024;
+    cache[device][0] = a;
+    cache[device][1] = b;
+  }
+  *per_sm = cache[device][0];
+  *reserved_per_cta = cache[device][1];
+}
+
 void set_launch_count(int n) { t_launches = n; }
 
 // Largest M served by the decode kernel when the path is automatic.

@@ -485,6 +485,21 @@ int fit_stages(const Geometry& g, uint32_t budget) {
   return s;
 }
 
+// Shared memory to request per CTA so that at most ceil(ctas / SMs) CTAs of
+// the launch fit on one SM.  Measured on GB300 over the Llama-3 8B/70B decode
+// shapes: when more CTAs fit than the even share, the block scheduler packs
+// clusters onto fewer SMs and the launch runs up to 1.5x slower; capping
+// residency at the even share keeps every SM's copy engine streaming.  The
+// padding is also the budget for ring stages.
+uint32_t residency_budget(int device, int ctas) {
+  int per_sm = 0, reserved = 0;
+  sm_shared_memory(device, &per_sm, &reserved);
+  const int sms = num_sms(device);
+  const int r = std::max(1, (ctas + sms - 1) / sms);
+  const int b = per_sm / r - reserved;
+  return (uint32_t)std::min<int>((int)kSmemPerCta, std::max(0, b)) & ~127u;
+}
+
 template <int MT, int WN, int NW, int UPS, bool XP>
 tm_status launch_t(const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem, cudaStream_t stream) {
   auto kern = decode_kernel<MT, WN, NW, UPS, XP>;
@@ -543,11 +558,11 @@ tm_status launch_m(int WN, int NW, int UPS, const CUtensorMap& tmX, const Decode
 
 }  // namespace
 
-// Launch shape.  Measured on GB300 over the Llama-3 8B/70B decode shapes: the
-// fastest shapes keep many small CTAs resident (256 or more per launch)
-// with shallow rings -- more consumer warps per SM beat deeper prefetch --
-// so the rule is: 128 columns per CTA (else 64, else 256), the smallest
-// cluster split giving at least 256 CTAs, 4 stages for M <= 16 and 2 above.
+// Launch shape.  Measured on GB300 over the Llama-3 8B/70B decode shapes:
+// 128 columns per CTA (else 64, else 256) and the smallest cluster split
+// giving at least 256 CTAs; shared memory padded so that each SM holds an
+// even share of the CTAs (residency_budget), and as many ring stages as that
+// budget holds, up to the CTA's super-group count.
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out) {
   const Layout& L = p->L;
   const int MT = mt_for(M);
@@ -586,8 +601,8 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
       if (want_S && S != want_S) continue;
       if (!want_S && S > 1 && S > L.NSG) break;
       const int per_cta = (L.NSG + S - 1) / S;
-      int stages = want_stages ? want_stages : std::min(MT <= 2 ? 3 : 2, std::max(2, per_cta));
-      if (!want_stages) stages = std::min(stages, std::max(2, fit_stages(g, kSmemPerCta)));
+      const uint32_t budget = residency_budget(p->device, NB * S);
+      int stages = want_stages ? want_stages : std::min(std::max(2, per_cta), std::max(2, fit_stages(g, budget)));
       if (stages < 2 || smem_bytes(g, stages) > kSmemPerCta) continue;
       const tm_gemm_config c = {1, S, tile, stages, wn};
       if (NB * S > fallback_ctas) {
@@ -649,8 +664,9 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   P.stage_bytes = g.stage;
   P.r_off = g.stage * c.stages;
   P.bar_off = (P.r_off + g.red + 15u) & ~15u;
-  const uint32_t smem = smem_bytes(g, c.stages);
-  if (smem > kSmemPerCta) return TM_ERR_UNSUPPORTED;
+  const uint32_t need = smem_bytes(g, c.stages);
+  if (need > kSmemPerCta) return TM_ERR_UNSUPPORTED;
+  const uint32_t smem = std::max(need, residency_budget(p->device, ((L.NT + CN - 1) / CN) * S));
   tm_status st;
   switch (MT) {
     case 1:

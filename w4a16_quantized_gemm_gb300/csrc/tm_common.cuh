@@ -105,6 +105,9 @@ cudaError_t prefill_error_bits(uint32_t* bits, bool clear);
 
 // Common host launch helpers (defined in api.cu).
 int num_sms(int device);
+// Shared memory of one SM that resident CTAs share, and the part of it the
+// system reserves for each CTA (bytes).
+void sm_shared_memory(int device, int* per_sm, int* reserved_per_cta);
 void set_launch_count(int n);
 
 // Decode / prefill launchers (decode.cu, prefill.cu).
