@@ -48,11 +48,13 @@ typedef struct tm_packed tm_packed;
 
 /* Optional launch settings for tm_w4a16_gemm_ex; zero fields mean "automatic". */
 typedef struct {
-  int path;    /* 0 auto, 1 decode kernel (mma.sync, M <= 64), 2 prefill kernel (tcgen05) */
+  int path;    /* 0 auto, 1 decode kernel (mma.sync, M <= 64), 2 prefill kernel (tcgen05, W^T staged in
+                  shared memory), 3 tensor-memory kernel (tcgen05, W^T dequantised into tensor memory) */
   int split_k; /* 0 auto, else number of CTAs (a thread-block cluster, 1..8) sharing one output tile along K */
-  int tile_n;  /* 0 auto, else output columns per CTA (decode 64/128/256, prefill 128/256) */
-  int stages;  /* 0 auto, else pipeline depth in shared memory (2..8) */
+  int tile_n;  /* 0 auto, else output columns per CTA (decode 64/128/256, prefill 256, tensor-memory 128) */
+  int stages;  /* 0 auto, else pipeline depth in shared memory (decode 2..8, prefill 6, tensor-memory 2..16) */
   int warp_n;  /* decode only: 0 auto, else 16-column tiles per consumer warp (1, 2 or 4) */
+  int tile_m;  /* tensor-memory path only: 0 auto, else rows of X per CTA (16, 32, 64, 128 or 256) */
 } tm_gemm_config;
 
 /* Human-readable name of a status (static string, never NULL). */
@@ -90,8 +92,9 @@ void tm_packed_free(tm_packed* p);
  * Y: device fp16 [M][N] row-major, 16-byte aligned, written in full.
  * stream: a cudaStream_t (NULL = the legacy default stream).
  * Asynchronous on `stream`; no host synchronisation, no allocation.
- * M <= 64 runs the decode kernel (split-K mma.sync GEMV/skinny GEMM),
- * larger M the tcgen05 prefill kernel.  Different calls may share a handle
+ * M <= 32 runs the decode kernel (split-K mma.sync GEMV/skinny GEMM),
+ * larger M the tcgen05 tensor-memory kernel (W^T dequantised into tensor
+ * memory as the MMA's A operand).  Different calls may share a handle
  * concurrently: a call keeps no state outside its own launch.
  */
 tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void* stream);

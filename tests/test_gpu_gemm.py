@@ -195,6 +195,6 @@ def test_prefill_split_override(split, K):
 
 def test_prefill_auto_split_small_m():
     w = packed(4096, 4096, 128)
-    assert binding.plan(w, 128)["split_k"] > 1
-    err, _ = run_and_compare(128, 4096, 4096, 128)
+    assert binding.plan(w, 128, {"path": 2})["split_k"] > 1
+    err, _ = run_and_compare(128, 4096, 4096, 128, config={"path": 2})
     assert err <= TOL, err

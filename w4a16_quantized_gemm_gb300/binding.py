@@ -31,7 +31,7 @@ class TMError(RuntimeError):
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_n", ctypes.c_int),
-                ("stages", ctypes.c_int), ("warp_n", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("warp_n", ctypes.c_int), ("tile_m", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -64,7 +64,9 @@ void sm_shared_memory(int device, int* per_sm, int* reserved_per_cta) {
 
 void set_launch_count(int n) { t_launches = n; }
 
-// Largest M served by the decode kernel when the path is automatic.
+// Largest M the decode kernel serves, and the largest it gets when the path
+// is automatic; above that the tensor-memory kernel runs (measured faster on
+// GB300 from M = 33 up).
 constexpr int kDecodeMaxM = 64;
 constexpr int kAutoDecodeMaxM = 32;
 
@@ -72,12 +74,13 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static tm_status plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out) {
   int path = cfg ? cfg->path : 0;
-  if (path == 0) path = M <= kAutoDecodeMaxM ? 1 : 2;
+  if (path == 0) path = M <= kAutoDecodeMaxM ? 1 : 3;
   if (path == 1) {
     if (M > kDecodeMaxM) return TM_ERR_UNSUPPORTED;
     return plan_decode(p, M, cfg, out);
   }
   if (path == 2) return plan_prefill(p, M, cfg, out);
+  if (path == 3) return plan_tc(p, M, cfg, out);
   return TM_ERR_INVALID_ARG;
 }
 
@@ -115,6 +118,7 @@ extern "C" tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y
   if (st != TM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (c.path == 1) return launch_decode(X, p, Y, M, c, s);
+  if (c.path == 3) return launch_tc(X, p, Y, M, c, s);
   return launch_prefill(X, p, Y, M, c, s);
 }
 
@@ -124,11 +128,11 @@ extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, i
 
 extern "C" tm_status tm_device_error(int clear, uint32_t* bits) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TM_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0;
   if (pack_error_bits(&a, clear != 0) != cudaSuccess || decode_error_bits(&b, clear != 0) != cudaSuccess ||
-      prefill_error_bits(&c, clear != 0) != cudaSuccess)
+      prefill_error_bits(&c, clear != 0) != cudaSuccess || tc_error_bits(&d, clear != 0) != cudaSuccess)
     return TM_ERR_CUDA;
-  const uint32_t v = (a | b | c) & kErrTimeout;
+  const uint32_t v = (a | b | c | d) & kErrTimeout;
   if (bits) *bits = v;
   return v ? TM_ERR_DEVICE_TIMEOUT : TM_OK;
 }

@@ -131,9 +131,10 @@ cudaError_t pack_error_bits(uint32_t* bits, bool clear) {
   return e;
 }
 
-// Tensor map without swizzle: dims[0] innermost, strides in bytes for dims 1..rank-1.
+// Tensor map (swizzle none unless asked): dims[0] innermost, strides in bytes for dims 1..rank-1.
 static bool encode_nd(CUtensorMap* map, CUtensorMapDataType dt, void* base, int rank, const uint64_t* dims,
-                      const uint64_t* strides, const uint32_t* box) {
+                      const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t d[5], st[4];
@@ -144,8 +145,8 @@ static bool encode_nd(CUtensorMap* map, CUtensorMapDataType dt, void* base, int 
     es[i] = 1;
     if (i + 1 < rank) st[i] = strides[i];
   }
-  CUresult r = fn(map, dt, (cuuint32_t)rank, base, d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(map, dt, (cuuint32_t)rank, base, d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -226,9 +227,23 @@ extern "C" tm_status tm_pack_weights(const uint8_t* q, const uint8_t* z, const u
   const uint64_t zd[3] = {16, (uint64_t)L.NT, (uint64_t)L.NSG};
   const uint64_t zs[2] = {16, (uint64_t)L.NT * 16};
   const uint32_t zb[3] = {16, 16, 1};
+  // Tensor-memory kernel, 8 n-tiles a box; a unit is viewed as 4 rows of
+  // 128 bytes (8 lanes each) so that the 128-byte swizzle applies:
+  //   codes  u32 {32, 4, UPS, NT, NSG} box {32, 4, 1, 8, 1}, 128-byte swizzle
+  //   scales u16 {16, 2, NT, NSG}      box {16, 1, 8, 1}
+  //   zeros  u8  {16, NT, NSG}         box {16, 8, 1}
+  const uint64_t td[5] = {32, 4, (uint64_t)L.UPS, (uint64_t)L.NT, (uint64_t)L.NSG};
+  const uint64_t ts[4] = {128, kUnitBytes, (uint64_t)L.UPS * kUnitBytes, (uint64_t)L.NT * L.UPS * kUnitBytes};
+  const uint32_t tb[5] = {32, 4, 1, 8, 1};
+  const uint32_t tsb[4] = {16, 1, 8, 1};
+  const uint32_t tzb[3] = {16, 8, 1};
   bool ok = encode_nd(&p->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, p->base + L.codes_off, 4, cd, cs, cb) &&
             encode_nd(&p->tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, p->base + L.scales_off, 4, sd, ss, sb) &&
-            encode_nd(&p->tm_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->base + L.zeros_off, 3, zd, zs, zb);
+            encode_nd(&p->tm_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->base + L.zeros_off, 3, zd, zs, zb) &&
+            encode_nd(&p->tc_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, p->base + L.codes_off, 5, td, ts, tb,
+                      CU_TENSOR_MAP_SWIZZLE_128B) &&
+            encode_nd(&p->tc_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, p->base + L.scales_off, 4, sd, ss, tsb) &&
+            encode_nd(&p->tc_zeros, CU_TENSOR_MAP_DATA_TYPE_UINT8, p->base + L.zeros_off, 3, zd, zs, tzb);
   if (!ok) {
     cudaFree(p->base);
     delete p;

@@ -396,6 +396,7 @@ tm_status plan_prefill(const tm_packed* p, int M, const tm_gemm_config* in, tm_g
   out->tile_n = tile_n;
   out->stages = kSA;
   out->warp_n = 0;
+  out->tile_m = 0;
   return TM_OK;
 }
 

@@ -76,10 +76,15 @@ struct tm_packed {
   w4::Layout L;
   int device;
   uint8_t* base;  // device allocation
-  // TMA descriptors over the packed regions (prefill kernel)
+  // TMA descriptors over the packed regions (prefill kernel: 16 n-tiles a box)
   CUtensorMap tm_codes;
   CUtensorMap tm_scales;
   CUtensorMap tm_zeros;
+  // The same for the tensor-memory kernel: 8 n-tiles a box, codes as 128-byte
+  // rows with the 128-byte swizzle (a conflict-free transposed read)
+  CUtensorMap tc_codes;
+  CUtensorMap tc_scales;
+  CUtensorMap tc_zeros;
 };
 
 namespace w4 {
@@ -102,6 +107,7 @@ EncodeTiledFn encode_tiled_fn();
 cudaError_t pack_error_bits(uint32_t* bits, bool clear);
 cudaError_t decode_error_bits(uint32_t* bits, bool clear);
 cudaError_t prefill_error_bits(uint32_t* bits, bool clear);
+cudaError_t tc_error_bits(uint32_t* bits, bool clear);
 
 // Common host launch helpers (defined in api.cu).
 int num_sms(int device);
@@ -117,6 +123,9 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
 tm_status plan_prefill(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);
 tm_status launch_prefill(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& cfg,
                          cudaStream_t stream);
+tm_status plan_tc(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);
+tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& cfg,
+                    cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Device helpers.
@@ -154,6 +163,23 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 constexpr uint32_t kSuspendHintNs = 200000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if defined(TM_WAIT_NOHINT)
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#elif defined(TM_WAIT_TEST)
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -161,6 +187,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
+#endif
   return ok != 0;
 }
 
@@ -214,6 +241,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
       "[%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+      "%6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
 
@@ -402,6 +438,36 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] . B[smem desc]^T, kind::f16, single CTA.  A occupies
+// tensor-memory lanes 0..127 (its rows) and 8 columns per 16 k (column c holds
+// k = 2c in the low half and 2c + 1 in the high half).
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 lanes x 8 columns: lane (4 gr + t) stores r0, r1 into tensor-memory lane
+// (base + gr) at columns 2t, 2t + 1 and r2, r3 into lane (base + gr + 8) at
+// the same columns -- the mma.m16n8 accumulator layout.
+__device__ __forceinline__ void tc_st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3));
+}
+
+// 32 lanes x 8 consecutive 32-bit columns: thread i gets lane (base lane + i).
+__device__ __forceinline__ void tc_ld_32x32b_x8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i).
 __device__ __forceinline__ void tc_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
