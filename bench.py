@@ -16,7 +16,7 @@ from HBM).  A step is captured once as a CUDA graph and replayed.
               workload, extrapolated to the full step, on the host cores.
 
 --workload prefill runs the Llama-3-8B prefill shapes (M in {128,1024,4096},
-TFLOP/s against the measured tensor peak) instead.
+TFLOP/s of the tensor-memory kernel against the measured tensor peak) instead.
 --impl reference times the oracle as the reference arm.
 """
 from __future__ import annotations
@@ -42,7 +42,7 @@ WORKLOADS = {
     "prefill": {"idx": 2, "unit": "TFLOP/s", "bound": "tensor",
                 "name": "llama3-8b prefill linears: qkv/o_proj/gate_up/down x M in {128,1024,4096}, g=128"},
 }
-KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "prefill": ["prefill.cu", "tm_common.cuh"]}
+KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "tc": ["tc.cu", "tm_common.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -303,7 +303,7 @@ def run_gpu(args, rank, world, local):
         per_rank_units = wl.step_flops * args.steps / 1e12
         achieved = wl.step_flops / step_s / 1e12
         peak = peaks["bf16_tflops_sustained"]
-        traffic = read_traffic("prefill", "llama3_8b_prefill")
+        traffic = read_traffic("tc", "llama3_8b_prefill")
         unit_kernel = "TFLOP/s"
     value = aggregate(per_rank_units, world, t_max_s)
 
@@ -317,13 +317,13 @@ def run_gpu(args, rank, world, local):
         "config": {"workload": spec["name"], "gemms_per_step": len(wl.items),
                    "bytes_per_step": wl.step_bytes, "flops_per_step": wl.step_flops,
                    "packed_weight_bytes_per_step": wl.weight_bytes,
-                   "accumulate": "f32", "launch": "one CUDA graph per step (16 kernel nodes)",
+                   "accumulate": "f32", "launch": f"one CUDA graph per step ({len(wl.items)} kernel nodes)",
                    "l2": "inputs larger than L2: every GEMM of a step has its own weights (>129 MB per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
                      "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peaks["source"],
-                     "kernel": "decode_kernel" if spec["bound"] == "hbm" else "prefill_kernel",
+                     "kernel": "decode_kernel" if spec["bound"] == "hbm" else "tc_kernel",
                      "basis": "algorithmic units of the step's launches / mean step time of the timed "
                               "region (CUDA events around each graph replay); consecutive launches overlap "
                               "under programmatic dependent launch, so the step time is their combined "
@@ -536,7 +536,8 @@ def main(argv=None):
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
     p.add_argument("--single", default=None, help="M,K,N,g: one GEMM 15 times, cold L2 (for ncu captures)")
-    p.add_argument("--path", type=int, default=0, help="with --single: 1 decode, 2 prefill, 0 automatic")
+    p.add_argument("--path", type=int, default=0,
+                   help="with --single: 1 decode, 2 prefill (shared-memory W^T), 3 tensor-memory, 0 automatic")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
