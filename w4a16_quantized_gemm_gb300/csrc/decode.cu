@@ -559,10 +559,11 @@ tm_status launch_m(int WN, int NW, int UPS, const CUtensorMap& tmX, const Decode
 }  // namespace
 
 // Launch shape.  Measured on GB300 over the Llama-3 8B/70B decode shapes:
-// 128 columns per CTA (else 64, else 256) and the smallest cluster split
-// giving at least 256 CTAs; shared memory padded so that each SM holds an
-// even share of the CTAs (residency_budget), and as many ring stages as that
-// budget holds, up to the CTA's super-group count.
+// 128 columns per CTA (64 for short K with few columns; else the other,
+// else 256) and the smallest cluster split giving at least 256 CTAs; shared
+// memory padded so that each SM holds an even share of the CTAs
+// (residency_budget), and as many ring stages as that budget holds, up to
+// the CTA's super-group count.
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out) {
   const Layout& L = p->L;
   const int MT = mt_for(M);
@@ -575,7 +576,11 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
   if (want_stages && (want_stages < 2 || want_stages > 8)) return TM_ERR_INVALID_ARG;
   if (want_wn && want_wn != 1 && want_wn != 2 && want_wn != 4) return TM_ERR_INVALID_ARG;
   constexpr int kMinCtas = 256;
-  const int tiles[3] = {128, 64, 256};
+  // 128 columns per CTA first, unless that needs a cluster of 8 CTAs that
+  // each hold fewer than 4 super-groups of K: then 64 columns (half the
+  // cluster, the same CTA count) measured faster.
+  const bool narrow = (L.NT + 7) / 8 * 4 < kMinCtas && L.NSG < 32;
+  const int tiles[3] = {narrow ? 64 : 128, narrow ? 128 : 64, 256};
   const int splits[4] = {1, 2, 4, 8};
   tm_gemm_config pick = {0, 0, 0, 0, 0};
   tm_gemm_config fallback = {0, 0, 0, 0, 0};  // the shape with the most CTAs
