@@ -3,7 +3,7 @@
 Default workload (the metric's headline configuration): the Llama-3-8B decode
 linear layers -- qkv (4096x6144), o_proj (4096x4096), gate_up (4096x28672),
 down (14336x4096) -- at M in {1, 8, 16, 32}, g = 128.  One step = those 16
-GEMMs, each with its own packed weights, X and Y (440 MB of distinct packed
+GEMMs, each with its own packed weights, X and Y (453 MB of distinct packed
 weights per step, more than the 129 MB L2, so every step streams its weights
 from HBM).  A step is captured once as a CUDA graph and replayed.
 
