@@ -497,6 +497,152 @@ def run_reference(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+def run_rtn(args, rank, world, local):
+    """--workload rtn: round-to-nearest INT4 quantisation (tm_quantize_rtn) of
+    the four Llama-3-8B linear weights (fp16 in; codes, zeros, scales out), one
+    step = the four layers, graph-replayed; GB/s of algorithmic bytes against
+    the measured HBM copy bandwidth."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    import oracle.rtn as rtn_oracle
+    from w4a16_quantized_gemm_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    peaks = load_peaks()
+    g = 128
+    layers = []
+    for name, (K, N) in synth.LLAMA3_8B.items():
+        Wh = synth.fp16_weights(K, N, g)
+        W = torch.from_numpy(Wh.view(np.uint16)).to(device).view(torch.float16)
+        q = torch.empty((K, N), dtype=torch.uint8, device=device)
+        z = torch.empty((K // g, N), dtype=torch.uint8, device=device)
+        sc = torch.empty((K // g, N), dtype=torch.float16, device=device)
+        layers.append({"name": name, "K": K, "N": N, "Wh": Wh, "W": W, "q": q, "z": z, "s": sc,
+                       "bytes": rtn_oracle.bytes_moved(K, N, g)})
+    step_bytes = sum(L["bytes"] for L in layers)
+    lib = binding.load()
+    stream = torch.cuda.Stream(device)
+
+    def launch_all(st):
+        for L in layers:
+            r = lib.tm_quantize_rtn(L["W"].data_ptr(), L["K"], L["N"], g, L["q"].data_ptr(), L["z"].data_ptr(),
+                                    L["s"].data_ptr(), ctypes.c_void_p(st.cuda_stream))
+            if r != 0:
+                raise RuntimeError(f"tm_quantize_rtn failed: {r}")
+
+    with torch.cuda.stream(stream):
+        launch_all(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        launch_all(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_sampler0 = time.time()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        evs[1].record(stream)
+    stream.synchronize()
+    t_ms = evs[0].elapsed_time(evs[1])
+    with torch.cuda.stream(stream):
+        while time.time() - t_sampler0 < 1.5:
+            for _ in range(50):
+                graph.replay()
+            stream.synchronize()
+    clocks = sampler.stop()
+    t_max_s = reduce_max(t_ms / 1e3, world)
+    value = aggregate(step_bytes * args.steps / 1e9, world, t_max_s)
+    achieved = step_bytes / (t_ms / 1e3 / args.steps) / 1e9
+
+    e2e = None
+    cpu = None
+    if rank == 0:
+        # public call with host buffers: pinned W in, quantise, codes/zeros/scales out
+        hostW = [torch.from_numpy(L["Wh"].view(np.uint16)).view(torch.float16).pin_memory() for L in layers]
+        outs = [(torch.empty(tuple(L["q"].shape), dtype=torch.uint8, pin_memory=True),
+                 torch.empty(tuple(L["z"].shape), dtype=torch.uint8, pin_memory=True),
+                 torch.empty(tuple(L["s"].shape), dtype=torch.float16, pin_memory=True)) for L in layers]
+        h2d = sum(w.numel() * 2 for w in hostW)
+        d2h = sum(a.numel() * a.element_size() for o in outs for a in o)
+        steps = max(3, min(args.steps, 20))
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            for w, o in zip(hostW, outs):
+                qd, zd, sd = binding.quantize_rtn(w.to(device, non_blocking=True), g)
+                o[0].copy_(qd, non_blocking=True)
+                o[1].copy_(zd, non_blocking=True)
+                o[2].copy_(sd, non_blocking=True)
+            torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        e2e = {"value": round(step_bytes / 1e9 * steps / dt, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt * 1e3 / steps, 3),
+               "timing": "host wall clock; W copied in, quantised, codes/zeros/scales copied out"}
+        if world == 1 and not args.no_cpu:
+            t0 = time.perf_counter()
+            for L in layers:
+                rtn_oracle.quantize(L["Wh"], g)
+            t_cpu = time.perf_counter() - t0
+            cpu = {"value": round(step_bytes / 1e9 / t_cpu, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"the whole step (four layers, numpy binary32 on one core), {t_cpu:.1f} s"}
+    out = {
+        "metric": "RTN INT4 quantisation GB/s (fp16 weights in, codes/zeros/scales out), Llama-3-8B linears",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "rtn: qkv/o_proj/gate_up/down fp16 weights, g=128", "launches_per_step": len(layers),
+                   "bytes_per_step": step_bytes,
+                   "l2": "inputs larger than L2 (698 MB of fp16 weights per step)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"], "kernel": "rtn_kernel"},
+        "gpu_launches": len(layers) * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_rtn_reference(args, rank):
+    """Reference arm of --workload rtn: the binary32 oracle on the host."""
+    if rank != 0:
+        return
+    import oracle.rtn as rtn_oracle
+    from w4a16_quantized_gemm_gb300 import synth
+    g = 128
+    W = {n: synth.fp16_weights(K, N, g) for n, (K, N) in synth.LLAMA3_8B.items()}
+    step_bytes = sum(rtn_oracle.bytes_moved(K, N, g) for (K, N) in synth.LLAMA3_8B.values())
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        rtn_oracle.quantize(W["o_proj"], g)
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for w in W.values():
+            rtn_oracle.quantize(w, g)
+    dt = time.perf_counter() - t0
+    v = round(step_bytes / 1e9 * steps / dt, 4)
+    print(json.dumps({"impl": "reference", "metric": "RTN INT4 quantisation GB/s (fp16 weights in, "
+                      "codes/zeros/scales out), Llama-3-8B linears", "value": v, "unit": "GB/s", "n_gpus": 1,
+                      "steps": steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / steps, 3),
+                      "higher_is_better": True, "data": "synthetic",
+                      "config": {"workload": "rtn: qkv/o_proj/gate_up/down fp16 weights, g=128"},
+                      "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                       "sample": f"{steps} whole steps"},
+                      "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+          flush=True)
+
+
 def run_single(spec_text, path):
     """One GEMM shape, launched 15 times with a 256 MB write between launches
     (cold L2) -- a small, bounded case for ncu captures."""
@@ -531,7 +677,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn"], default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
@@ -548,7 +694,10 @@ def main(argv=None):
     if world != args.gpus and "RANK" in os.environ:
         p.error(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        if args.workload == "rtn":
+            run_rtn_reference(args, rank)
+        else:
+            run_reference(args, rank, world)
         return
     if world > 1:
         import torch
@@ -556,7 +705,10 @@ def main(argv=None):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     try:
-        run_gpu(args, rank, world, local)
+        if args.workload == "rtn":
+            run_rtn(args, rank, world, local)
+        else:
+            run_gpu(args, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -84,6 +84,26 @@ tm_status tm_unpack_weights(const tm_packed* p, uint8_t* q, uint8_t* z, uint16_t
 /* K, N, g and the size of the device allocation of a handle (any out pointer may be NULL). */
 tm_status tm_packed_info(const tm_packed* p, int* K, int* N, int* g, size_t* bytes);
 
+/*
+ * Round-to-nearest INT4 quantisation ("LMDeploy, in depth", section
+ * "Quantization: AWQ weights and KV cache": naive RTN INT4 is the baseline the
+ * pages compare AWQ against), producing exactly the inputs of tm_pack_weights.
+ * For every group G of g rows along K and column n, in IEEE binary32 with
+ * round-to-nearest-even at each step:
+ *   lo = min(0, min w), hi = max(0, max w); r = hi - lo, or 15 if r == 0
+ *   s[G][n] = fp16(r / 15), at least 2^-24 (the smallest positive fp16)
+ *   z[G][n] = clamp(rint(-lo / s), 0, 15);  i = 1 / s (once per group and column)
+ *   q[k][n] = clamp(rint(w[k][n] * i) + z, 0, 15)
+ *   W : device, fp16 bits [K][N] row-major, 16-byte aligned
+ *   q : device, uint8 [K][N] (one code per byte), 8-byte aligned
+ *   z : device, uint8 [K/g][N], 8-byte aligned;  s: device, fp16 bits [K/g][N], 16-byte aligned
+ * K % g == 0, N % 16 == 0, K/g <= 65535.  Asynchronous on `stream` (one launch,
+ * no allocation); the caller owns every buffer.  TM_ERR_INVALID_ARG on a bad
+ * shape or NULL pointer, TM_ERR_ALIGNMENT on a misaligned pointer.
+ */
+tm_status tm_quantize_rtn(const uint16_t* W, int K, int N, int g, uint8_t* q, uint8_t* z, uint16_t* s,
+                          void* stream);
+
 /* Release a handle and its device memory (NULL is ignored). */
 void tm_packed_free(tm_packed* p);
 

@@ -1,0 +1,82 @@
+"""GPU parity of the round-to-nearest INT4 quantiser (tm_quantize_rtn) against
+the binary32 oracle (oracle/rtn.py): codes, zeros and scales bit-exact, then
+the whole pipeline quantise -> pack -> GEMM against the fp64 GEMM oracle on the
+oracle's own codes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.rtn as rtn
+from tests.gpu_util import TOL
+from w4a16_quantized_gemm_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+
+def _gpu_quantize(W16, g):
+    Wd = torch.from_numpy(W16.view(np.uint16)).cuda().view(torch.float16)
+    q, z, s = binding.quantize_rtn(Wd, g)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), z.cpu().numpy(), s.cpu().numpy().view(np.uint16)
+
+
+def _assert_bit_exact(W16, g):
+    q, z, s = _gpu_quantize(W16, g)
+    q0, z0, s0 = rtn.quantize(W16, g)
+    assert np.array_equal(s, s0.view(np.uint16))
+    assert np.array_equal(z, z0)
+    assert np.array_equal(q, q0)
+
+
+@pytest.mark.parametrize("K,N,g", [(4096, 4096, 128), (4096, 6144, 128), (14336, 4096, 128), (4096, 28672, 128),
+                                   (4096, 28672, 64), (192, 48, 64), (128, 16, 128), (256, 272, 32), (512, 64, 256)])
+def test_rtn_bit_exact(K, N, g):
+    _assert_bit_exact(synth.fp16_weights(K, N, g), g)
+
+
+def test_rtn_special_values_bit_exact():
+    """Ties, degenerate groups, subnormal and largest fp16 magnitudes, signed zeros."""
+    T = np.array([-7.5, 7.5, 2.5, 3.5, -0.5, -6.5, 0.0, 1.0], dtype=np.float16)
+    cols = [np.repeat(T, 2), np.zeros(16, np.float16), np.full(16, 0.75, np.float16),
+            np.full(16, -0.375, np.float16), np.array([6e-8, -6e-8] * 8, np.float16),
+            np.array([65504, -65504] + [1.0] * 14, np.float16), np.array([-0.0, 0.0] * 8, np.float16),
+            np.linspace(-3, 5, 16).astype(np.float16)]
+    W = np.stack(cols + cols, axis=1)  # 16 columns
+    _assert_bit_exact(np.ascontiguousarray(W), 16)
+    _assert_bit_exact(np.ascontiguousarray(W), 8)
+
+
+def test_rtn_quantize_pack_gemm_pipeline():
+    K, N, g, M = 4096, 1024, 128, 8
+    W16 = synth.fp16_weights(K, N, g)
+    Wd = torch.from_numpy(W16.view(np.uint16)).cuda().view(torch.float16)
+    q, z, s = binding.quantize_rtn(Wd, g)
+    w = binding.pack(q, z, s, g)
+    X = synth.activations(M, K, tag="/rtn")
+    Xd = torch.from_numpy(X.view(np.uint16)).cuda().view(torch.float16)
+    Y = binding.gemm(Xd, w).float().cpu().numpy().astype(np.float64)
+    q0, z0, s0 = rtn.quantize(W16, g)
+    Y_ref = oracle.gemm(X, q0, z0, s0, g)
+    assert oracle.rel_max_err(Y, Y_ref) <= TOL
+    assert binding.device_error() == 0
+
+
+def test_rtn_rejects_bad_arguments():
+    W = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.TMError) as e:
+        binding.quantize_rtn(W, 96)          # K % g
+    assert e.value.status == 1
+    with pytest.raises(binding.TMError) as e:
+        binding.quantize_rtn(W[:, :40], 64)  # N % 16 (non-contiguous slice is copied first)
+    assert e.value.status == 1
+
+
+def test_rtn_one_launch():
+    W = torch.zeros((256, 64), dtype=torch.float16, device="cuda")
+    binding.quantize_rtn(W, 64)
+    assert binding.last_launch_count() == 1
+    torch.cuda.synchronize()

@@ -20,7 +20,7 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
-           "tm_last_launch_count")
+           "tm_last_launch_count", "tm_quantize_rtn")
 
 
 class TMError(RuntimeError):
@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
     lib.tm_device_error.argtypes = [ci, ctypes.POINTER(ctypes.c_uint32)]
     lib.tm_last_launch_count.restype = ci
     lib.tm_last_launch_count.argtypes = []
+    lib.tm_quantize_rtn.restype = ci
+    lib.tm_quantize_rtn.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -215,6 +217,25 @@ def _gemm_host(X, w, out, config, stream):
         out.copy_(Yd, non_blocking=True)
     s.synchronize()
     return out
+
+
+def quantize_rtn(W: torch.Tensor, g: int, stream: Optional[torch.cuda.Stream] = None):
+    """Round-to-nearest INT4 quantisation of fp16 W [K][N] on the GPU:
+    returns (q uint8 [K][N], z uint8 [K/g][N], s fp16 [K/g][N]), the inputs of
+    ``pack``.  Asynchronous on ``stream`` (default: the current stream)."""
+    if W.dim() != 2 or W.dtype != torch.float16:
+        raise ValueError("W must be fp16 [K][N]")
+    K, N = W.shape
+    Wd = W.contiguous()
+    _dev(Wd, torch.float16, "W")
+    q = torch.empty((K, N), dtype=torch.uint8, device=Wd.device)
+    z = torch.empty((K // g if g > 0 else 0, N), dtype=torch.uint8, device=Wd.device)
+    s = torch.empty((K // g if g > 0 else 0, N), dtype=torch.float16, device=Wd.device)
+    st = stream if stream is not None else torch.cuda.current_stream(Wd.device)
+    with torch.cuda.device(Wd.device):
+        _check(load().tm_quantize_rtn(Wd.data_ptr(), K, N, g, q.data_ptr(), z.data_ptr(), s.data_ptr(),
+                                      ctypes.c_void_p(st.cuda_stream)), "tm_quantize_rtn")
+    return q, z, s
 
 
 def device_error(clear: bool = True) -> int:

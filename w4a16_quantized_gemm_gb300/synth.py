@@ -160,6 +160,21 @@ def problem(M: int, K: int, N: int, g: int = 128, stress: bool = False, seed: in
 # The workloads: Llama-3-8B and Llama-3-70B linear-layer shapes.
 # (K, N): qkv = (hidden, hidden + 2*kv_heads*head_dim), o_proj = (hidden, hidden),
 # gate_up = (hidden, 2*intermediate), down = (intermediate, hidden).
+def fp16_weights(K: int, N: int, g: int = 128, seed: int = 0) -> np.ndarray:
+    """Dense fp16 weights [K][N] for the round-to-nearest quantiser: N(0,1)
+    times a per-column scale uniform in [0.005, 0.05] (a trained layer's
+    spread), rounded to fp16.  The first column's first group is all zeros and
+    the second column's first group constant (the quantiser's degenerate
+    cases) when the shape has them."""
+    tag = f"w16/K{K}/N{N}/g{g}/s{seed}"
+    col = scales64(tag + "/col", 1, N, 0.005, 0.05)
+    W = (normal64(tag, K, N) * col).astype(np.float16)
+    if K >= g and N >= 2:
+        W[:g, 0] = 0
+        W[:g, 1] = np.float16(0.0123)
+    return W
+
+
 LLAMA3_8B = {"qkv": (4096, 6144), "o_proj": (4096, 4096), "gate_up": (4096, 28672),
              "down": (14336, 4096)}
 LLAMA3_70B = {"qkv": (8192, 10240), "o_proj": (8192, 8192), "gate_up": (8192, 57344),
