@@ -614,6 +614,99 @@ def run_rtn(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def run_silu(args, rank, world, local):
+    """--workload silu: the Llama-3-8B gate_up layer (4096 x 28672, g=128) with
+    the fused silu(gate) * up epilogue (tm_w4a16_gemm_silu_mul) at the decode
+    sizes M in {1, 8, 16, 32}, one step = the four launches, graph-replayed;
+    GB/s of algorithmic bytes (W4 weights, X in, H out) against the measured
+    HBM bandwidth.  `unfused_ms_per_step` times the same step as GEMM + a
+    separate torch silu-mul pass, for context."""
+    import numpy as np
+    import torch
+    import torch.nn.functional as F
+
+    from w4a16_quantized_gemm_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    peaks = load_peaks()
+    K, N, g = synth.LLAMA3_8B["gate_up"][0], synth.LLAMA3_8B["gate_up"][1], 128
+    q, z, s, _ = synth.weights(K, N, g)
+    items = []
+    Ms = (1, 8, 16, 32)
+    for M in Ms:
+        w = binding.pack(torch.from_numpy(q).to(device), torch.from_numpy(z).to(device),
+                         torch.from_numpy(s.view(np.uint16)).to(device).view(torch.float16), g)
+        X = torch.from_numpy(synth.activations(M, K, tag=f"/silu/M{M}").view(np.uint16)).to(device).view(torch.float16)
+        items.append({"M": M, "w": w, "X": X, "H": torch.empty((M, N // 2), dtype=torch.float16, device=device),
+                      "Y": torch.empty((M, N), dtype=torch.float16, device=device),
+                      "bytes": K * N // 2 + (K // g) * N * 5 // 2 + 2 * M * K + 2 * M * (N // 2)})
+    step_bytes = sum(it["bytes"] for it in items)
+    stream = torch.cuda.Stream(device)
+
+    def fused(st):
+        for it in items:
+            binding.gemm_silu_mul(it["X"], it["w"], out=it["H"], stream=st)
+
+    def unfused(st):
+        for it in items:
+            binding.gemm(it["X"], it["w"], out=it["Y"], stream=st)
+            y = it["Y"].view(it["M"], N // 8, 2, 4)
+            it["H"].view(it["M"], N // 8, 4).copy_(F.silu(y[:, :, 0, :].float()).mul_(y[:, :, 1, :].float()))
+
+    def timed(fn, steps):
+        with torch.cuda.stream(stream):
+            fn(stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1), graph
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    t_ms, graph = timed(fused, args.steps)
+    with torch.cuda.stream(stream):
+        while time.time() - t0 < 1.5:
+            for _ in range(50):
+                graph.replay()
+            stream.synchronize()
+    clocks = sampler.stop()
+    t_unfused, _ = timed(unfused, args.steps)
+    t_max_s = reduce_max(t_ms / 1e3, world)
+    value = aggregate(step_bytes * args.steps / 1e9, world, t_max_s)
+    achieved = step_bytes / (t_ms / 1e3 / args.steps) / 1e9
+    out = {
+        "metric": "fused gate_up + silu*mul W4A16 GB/s, Llama-3-8B gate_up (4096 x 28672), M in {1,8,16,32}",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "silu: gate_up with fused silu(gate)*up epilogue", "launches_per_step": len(items),
+                   "bytes_per_step": step_bytes, "unfused_ms_per_step": round(t_unfused / args.steps, 4),
+                   "unfused": "the same GEMMs writing Y [M][N], then torch silu-mul on the interleaved halves",
+                   "l2": "each GEMM has its own packed weights (235 MB per step > 129 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"], "kernel": "decode_kernel / tc_kernel (fused epilogue)"},
+        "gpu_launches": len(items) * args.steps, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_rtn_reference(args, rank):
     """Reference arm of --workload rtn: the binary32 oracle on the host."""
     if rank != 0:
@@ -677,7 +770,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn"], default="decode")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu"], default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
@@ -696,6 +789,10 @@ def main(argv=None):
     if args.impl == "reference":
         if args.workload == "rtn":
             run_rtn_reference(args, rank)
+        elif args.workload == "silu":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the silu workload's reference arm is the "
+                                  "oracle timed by the default decode workload"}), flush=True)
         else:
             run_reference(args, rank, world)
         return
@@ -707,6 +804,8 @@ def main(argv=None):
     try:
         if args.workload == "rtn":
             run_rtn(args, rank, world, local)
+        elif args.workload == "silu":
+            run_silu(args, rank, world, local)
         else:
             run_gpu(args, rank, world, local)
     finally:

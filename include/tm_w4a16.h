@@ -119,6 +119,20 @@ void tm_packed_free(tm_packed* p);
  */
 tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void* stream);
 
+/*
+ * Fused gate/up product of a Llama MLP: H = silu(X . W_gate) * (X . W_up)
+ * in one launch, silu(x) = x / (1 + exp(-x)) in fp32 on the fp32 sums.
+ * The packed weight holds both halves with N = 2 I columns interleaved in
+ * blocks of 4 (our convention): columns 8b .. 8b+3 are gate columns
+ * 4b .. 4b+3 and columns 8b+4 .. 8b+7 the matching up columns.
+ *   H: device fp16 [M][N/2] row-major, 16-byte aligned; H[m][4b + i] pairs
+ *      W columns 8b + i (gate) and 8b + 4 + i (up).
+ * Same paths, planning and status codes as tm_w4a16_gemm_ex (cfg may be NULL);
+ * path 2 (shared-memory prefill kernel) returns TM_ERR_UNSUPPORTED.
+ */
+tm_status tm_w4a16_gemm_silu_mul(const void* X, const tm_packed* p, void* H, int M, const tm_gemm_config* cfg,
+                                 void* stream);
+
 /* tm_w4a16_gemm with explicit launch settings (cfg may be NULL = automatic). */
 tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config* cfg,
                            void* stream);

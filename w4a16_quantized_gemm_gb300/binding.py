@@ -20,7 +20,7 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
-           "tm_last_launch_count", "tm_quantize_rtn")
+           "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul")
 
 
 class TMError(RuntimeError):
@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
     lib.tm_device_error.argtypes = [ci, ctypes.POINTER(ctypes.c_uint32)]
     lib.tm_last_launch_count.restype = ci
     lib.tm_last_launch_count.argtypes = []
+    lib.tm_w4a16_gemm_silu_mul.restype = ci
+    lib.tm_w4a16_gemm_silu_mul.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
     lib.tm_quantize_rtn.restype = ci
     lib.tm_quantize_rtn.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp]
     _lib = lib
@@ -204,6 +206,27 @@ def gemm(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = None, 
         st = lib.tm_w4a16_gemm_ex(X.data_ptr(), w.handle, out.data_ptr(), M, ctypes.byref(c),
                                   ctypes.c_void_p(s.cuda_stream))
     _check(st, "tm_w4a16_gemm")
+    return out
+
+
+def gemm_silu_mul(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = None, config=None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """H = silu(X . W_gate) * (X . W_up) from one packed gate/up weight whose
+    columns interleave gate and up in blocks of 4 (see tm_w4a16_gemm_silu_mul).
+    X: CUDA fp16 [M][K]; returns fp16 [M][N/2]; asynchronous on ``stream``."""
+    if X.dim() != 2 or X.shape[1] != w.K or X.dtype != torch.float16 or not X.is_cuda:
+        raise ValueError("X must be a CUDA fp16 [M][K] tensor")
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N // 2), dtype=torch.float16, device=X.device)
+    elif out.shape != (M, w.N // 2) or out.dtype != torch.float16 or not out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous CUDA fp16 [M][N/2] tensor")
+    X = X.contiguous()
+    s = stream if stream is not None else torch.cuda.current_stream(X.device)
+    c = _cfg(config)
+    _check(load().tm_w4a16_gemm_silu_mul(X.data_ptr(), w.handle, out.data_ptr(), M,
+                                         ctypes.byref(c) if c else None, ctypes.c_void_p(s.cuda_stream)),
+           "tm_w4a16_gemm_silu_mul")
     return out
 
 

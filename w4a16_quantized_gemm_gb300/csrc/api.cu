@@ -122,6 +122,23 @@ extern "C" tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y
   return launch_prefill(X, p, Y, M, c, s);
 }
 
+extern "C" tm_status tm_w4a16_gemm_silu_mul(const void* X, const tm_packed* p, void* H, int M,
+                                            const tm_gemm_config* cfg, void* stream) {
+  t_launches = 0;
+  if (!p || M < 0) return TM_ERR_INVALID_ARG;
+  if (p->L.N % 8 != 0) return TM_ERR_INVALID_ARG;
+  if (M == 0) return TM_OK;
+  if (!X || !H) return TM_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(H)) return TM_ERR_ALIGNMENT;
+  tm_gemm_config c;
+  tm_status st = plan(p, M, cfg, &c);
+  if (st != TM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (c.path == 1) return launch_decode(X, p, H, M, c, s, true);
+  if (c.path == 3) return launch_tc(X, p, H, M, c, s, true);
+  return TM_ERR_UNSUPPORTED;  // the shared-memory prefill kernel has no fused epilogue
+}
+
 extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void* stream) {
   return tm_w4a16_gemm_ex(X, p, Y, M, nullptr, stream);
 }

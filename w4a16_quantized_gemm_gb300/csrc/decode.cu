@@ -52,6 +52,7 @@ struct DecodeParams {
   uint32_t stage_bytes;  // bytes per stage (1024-aligned)
   uint32_t r_off;        // offset of the reduction buffer
   uint32_t bar_off;      // offset of the barriers
+  int silu;              // Y = silu(gate) * up, [M][N/2] (gate/up interleaved in blocks of 4 columns)
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity) {
@@ -396,8 +397,34 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
   const int span = CNN / S;
   const uint32_t my_rank = S > 1 ? cluster_ctarank() : 0u;
   const int half_span = span >> 1;
-  const int items = P.M * half_span;
   const int n_base = nt0 * 16 + (int)my_rank * span;
+  if (P.silu) {
+    // Output column j of the slice pairs gate column 8(j/4) + j%4 with the up
+    // column 4 later (a slice is a multiple of 8 columns); two outputs a thread.
+    const int pairs = span >> 2;
+    const int Nh = P.N >> 1;
+    for (int it = threadIdx.x; it < P.M * pairs; it += blockDim.x) {
+      const int m = it / pairs;
+      const int j = 2 * (it - m * pairs);
+      const int c = 8 * (j >> 2) + (j & 3);
+      if (n_base + c >= P.N) continue;
+      float2 gt = make_float2(0.f, 0.f), up = make_float2(0.f, 0.f);
+#pragma unroll 8
+      for (int r = 0; r < S; ++r) {
+        const float* row = red + (r * (MT * 8) + m) * span;
+        const float2 a = *reinterpret_cast<const float2*>(row + c);
+        const float2 b = *reinterpret_cast<const float2*>(row + c + 4);
+        gt.x += a.x;
+        gt.y += a.y;
+        up.x += b.x;
+        up.y += b.y;
+      }
+      *reinterpret_cast<__half2*>(P.Y + (size_t)m * Nh + (n_base >> 1) + j) =
+          __floats2half2_rn(silu_mul(gt.x, up.x), silu_mul(gt.y, up.y));
+    }
+    return;
+  }
+  const int items = P.M * half_span;
   for (int it = threadIdx.x; it < items; it += blockDim.x) {
     const int m = it / half_span;
     const int col = 2 * (it - m * half_span);
@@ -628,7 +655,7 @@ tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_ge
 }
 
 tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& c,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool silu) {
   const Layout& L = p->L;
   const int MT = mt_for(M);
   int WN = 0, NW = 0;
@@ -667,6 +694,7 @@ tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const
   P.x_box = g.xp ? (uint32_t)M * 128u : (uint32_t)MT * 1024u;
   P.c_off = g.c_off;
   P.stage_bytes = g.stage;
+  P.silu = silu ? 1 : 0;
   P.r_off = g.stage * c.stages;
   P.bar_off = (P.r_off + g.red + 15u) & ~15u;
   const uint32_t need = smem_bytes(g, c.stages);

@@ -66,6 +66,7 @@ struct TcParams {
   int kb_per_cta;  // 64-k units per CTA of a cluster (a multiple of KU)
   int stages;      // ring slots
   uint32_t bar_off;
+  int silu;        // Y = silu(gate) * up, [M][N/2] (gate/up interleaved in blocks of 4 columns)
 };
 
 __device__ __forceinline__ bool tc_wait_time_only(uint32_t bar, uint32_t parity) {
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   bool acc_ok = true;
   if (epi) {
     acc_ok = mbar_wait(bar_acc, 0, abort_flag, &s_err_tc);
+    acc_ok = __all_sync(0xffffffffu, acc_ok);  // warp-uniform: the epilogue shuffles
     tc_fence_after();
   }
   if (S == 1) {
@@ -298,7 +300,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint32_t v[8];
         tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c), v);
         tc_wait_ld();
-        if (n < P.N) {
+        if (P.silu) {
+          // lanes with (n & 4) == 0 hold gate columns; their up columns sit 4 lanes higher
+          float up[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) up[e] = __shfl_down_sync(0xffffffffu, __uint_as_float(v[e]), 4);
+          if (n < P.N && (n & 4) == 0) {
+            const int j = 4 * (n >> 3) + (n & 3);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int m = m0 + h * HALF + c + e;
+              if (m < P.M) P.Y[(size_t)m * (P.N >> 1) + j] = __float2half_rn(silu_mul(__uint_as_float(v[e]), up[e]));
+            }
+          }
+        } else if (n < P.N) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
             const int m = m0 + h * HALF + c + e;
@@ -335,7 +350,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dependency_wait();
     const float* red = reinterpret_cast<const float*>(smem);
     const int n_base = nt0 * 16 + (int)my_rank * R;
-    for (int it = threadIdx.x; it < R * BT; it += blockDim.x) {
+    if (P.silu) {
+      // output jj of the rank's R columns pairs gate column 8(jj/4) + jj%4 with the one 4 later
+      const int R2 = R >> 1;
+      for (int it = threadIdx.x; it < R2 * BT; it += blockDim.x) {
+        const int tok = it / R2, jj = it - tok * R2;
+        const int rr = 8 * (jj >> 2) + (jj & 3);
+        const int m = m0 + tok, n = n_base + rr;
+        if (m >= P.M || n >= P.N) continue;
+        float gt = 0.f, up = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < S; ++k) {
+          gt += red[(k * R + rr) * BT + tok];
+          up += red[(k * R + rr + 4) * BT + tok];
+        }
+        P.Y[(size_t)m * (P.N >> 1) + (n_base >> 1) + jj] = __float2half_rn(silu_mul(gt, up));
+      }
+    }
+    for (int it = threadIdx.x; it < (P.silu ? 0 : R * BT); it += blockDim.x) {
       const int tok = it / R, rr = it - tok * R;
       const int m = m0 + tok, n = n_base + rr;
       if (m >= P.M || n >= P.N) continue;
@@ -504,7 +536,7 @@ tm_status plan_tc(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_c
 }
 
 tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& c,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, bool silu) {
   const Layout& L = p->L;
   const int BT = c.tile_m;
   TcVariant v;
@@ -535,6 +567,7 @@ tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_
   P.kb_per_cta = ((rounds + S - 1) / S) * v.KU;
   P.stages = c.stages;
   P.bar_off = tc_bar_off(v, c.stages);
+  P.silu = silu ? 1 : 0;
   if (tc_smem_need(v, c.stages) > kTcSmemMax) return TM_ERR_UNSUPPORTED;
   const uint32_t smem = tc_smem_request(p->device, v, c.stages);
   tm_status st = TM_ERR_UNSUPPORTED;

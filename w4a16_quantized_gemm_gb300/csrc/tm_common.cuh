@@ -119,13 +119,13 @@ void set_launch_count(int n);
 // Decode / prefill launchers (decode.cu, prefill.cu).
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);
 tm_status launch_decode(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& cfg,
-                        cudaStream_t stream);
+                        cudaStream_t stream, bool silu = false);
 tm_status plan_prefill(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);
 tm_status launch_prefill(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& cfg,
                          cudaStream_t stream);
 tm_status plan_tc(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);
 tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config& cfg,
-                    cudaStream_t stream);
+                    cudaStream_t stream, bool silu = false);
 
 // ---------------------------------------------------------------------------
 // Device helpers.
@@ -385,6 +385,12 @@ __device__ __forceinline__ void grid_dependency_wait() {
 // Allow the next grid in the stream to begin launching.
 __device__ __forceinline__ void launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// silu(gate) * up for the fused gate/up epilogue, in fp32 (expf and an IEEE
+// division; silu(x) = x / (1 + exp(-x))).
+__device__ __forceinline__ float silu_mul(float gate, float up) {
+  return __fdiv_rn(gate, 1.f + expf(-gate)) * up;
 }
 
 // ---- tcgen05 --------------------------------------------------------------
