@@ -145,6 +145,13 @@ tm_status tm_gemm_plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_
  * clear != 0 resets them.  Returns TM_ERR_DEVICE_TIMEOUT when bit 0 was set. */
 tm_status tm_device_error(int clear, uint32_t* bits);
 
+/* Self-test of the bounded barrier waits (failure detection without a fault):
+ * launches one warp that waits on a barrier nothing arrives on; after about
+ * one second the wait gives up, sets bit 0 and the kernel returns, leaving
+ * the context usable.  Asynchronous on `stream`; read the outcome with
+ * tm_device_error (expected: TM_ERR_DEVICE_TIMEOUT, bits == 1). */
+tm_status tm_selftest_wait_timeout(void* stream);
+
 /* Number of kernel launches the last tm_w4a16_gemm* call on this thread made (1 or 0). */
 int tm_last_launch_count(void);
 

@@ -20,7 +20,7 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
-           "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul")
+           "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout")
 
 
 class TMError(RuntimeError):
@@ -78,6 +78,8 @@ def load(path: Optional[str] = None):
     lib.tm_device_error.argtypes = [ci, ctypes.POINTER(ctypes.c_uint32)]
     lib.tm_last_launch_count.restype = ci
     lib.tm_last_launch_count.argtypes = []
+    lib.tm_selftest_wait_timeout.restype = ci
+    lib.tm_selftest_wait_timeout.argtypes = [vp]
     lib.tm_w4a16_gemm_silu_mul.restype = ci
     lib.tm_w4a16_gemm_silu_mul.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
     lib.tm_quantize_rtn.restype = ci
@@ -259,6 +261,12 @@ def quantize_rtn(W: torch.Tensor, g: int, stream: Optional[torch.cuda.Stream] = 
         _check(load().tm_quantize_rtn(Wd.data_ptr(), K, N, g, q.data_ptr(), z.data_ptr(), s.data_ptr(),
                                       ctypes.c_void_p(st.cuda_stream)), "tm_quantize_rtn")
     return q, z, s
+
+
+def selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Launch the bounded-wait self-test (see tm_selftest_wait_timeout)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(load().tm_selftest_wait_timeout(ctypes.c_void_p(s.cuda_stream)), "tm_selftest_wait_timeout")
 
 
 def device_error(clear: bool = True) -> int:

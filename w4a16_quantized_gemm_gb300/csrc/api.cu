@@ -84,9 +84,31 @@ static tm_status plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_g
   return TM_ERR_INVALID_ARG;
 }
 
+// Self-test of the bounded barrier wait every kernel uses: one warp waits on
+// an mbarrier that nothing ever arrives on; after kWaitLimitNs it must give
+// up, raise the abort flag and set the timeout bit, and the kernel returns.
+static __device__ uint32_t s_err_selftest;
+
+__global__ void wait_timeout_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(smem_u32(&bar), 0, reinterpret_cast<volatile int*>(&abort_flag), &s_err_selftest);
+}
+
 }  // namespace w4
 
 using namespace w4;
+
+extern "C" tm_status tm_selftest_wait_timeout(void* stream) {
+  wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  return cudaGetLastError() == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+}
 
 extern "C" const char* tm_status_str(tm_status s) {
   switch (s) {
@@ -145,11 +167,16 @@ extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, i
 
 extern "C" tm_status tm_device_error(int clear, uint32_t* bits) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TM_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, d = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0, e = 0;
   if (pack_error_bits(&a, clear != 0) != cudaSuccess || decode_error_bits(&b, clear != 0) != cudaSuccess ||
-      prefill_error_bits(&c, clear != 0) != cudaSuccess || tc_error_bits(&d, clear != 0) != cudaSuccess)
+      prefill_error_bits(&c, clear != 0) != cudaSuccess || tc_error_bits(&d, clear != 0) != cudaSuccess ||
+      cudaMemcpyFromSymbol(&e, s_err_selftest, sizeof(e)) != cudaSuccess)
     return TM_ERR_CUDA;
-  const uint32_t v = (a | b | c | d) & kErrTimeout;
+  if (clear && e) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(s_err_selftest, &zero, sizeof(zero)) != cudaSuccess) return TM_ERR_CUDA;
+  }
+  const uint32_t v = (a | b | c | d | e) & kErrTimeout;
   if (bits) *bits = v;
   return v ? TM_ERR_DEVICE_TIMEOUT : TM_OK;
 }
