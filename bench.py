@@ -707,6 +707,107 @@ def run_silu(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def run_kv(args, rank, world, local):
+    """--workload kv: decode attention over a low-bit KV cache
+    (tm_kv_decode_attention), Llama-3-8B heads (32 query / 8 KV heads, D = 128),
+    32 sequences x 4096 cached tokens, one step = the int8 and the int4 cache
+    (two launches), graph-replayed; GB/s of algorithmic bytes (codes, scales and
+    zeros of K and V, Q in, out) against the measured HBM bandwidth."""
+    import numpy as np
+    import torch
+
+    import oracle.kv as kv_oracle
+    from w4a16_quantized_gemm_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    peaks = load_peaks()
+    Bsz, L, Hq, Hkv, D = 32, 4096, 32, 8, 128
+    lens = torch.full((Bsz,), L, dtype=torch.int32, device=device)
+    Q = torch.from_numpy(synth.normal64("kvbench/Q", 1, Bsz * Hq * D).reshape(Bsz, Hq, D)
+                         .astype(np.float16).view(np.uint16)).to(device).view(torch.float16)
+    caches = []
+    for bits in (8, 4):
+        K = torch.randn((Bsz, L, Hkv, D), generator=torch.Generator(device=device).manual_seed(bits),
+                        device=device, dtype=torch.float32).half()
+        V = torch.randn((Bsz, L, Hkv, D), generator=torch.Generator(device=device).manual_seed(100 + bits),
+                        device=device, dtype=torch.float32).half()
+        caches.append((bits, binding.kv_quantize(K, bits), binding.kv_quantize(V, bits),
+                       torch.empty((Bsz, Hq, D), dtype=torch.float16, device=device)))
+        del K, V
+    step_bytes = sum(kv_oracle.cache_bytes(Bsz, L, Hkv, D, bits) for bits in (8, 4)) + 2 * 2 * Bsz * Hq * D * 2
+    stream = torch.cuda.Stream(device)
+
+    def launch_all(st):
+        for bits, kq, vq, out in caches:
+            binding.kv_decode_attention(Q, kq, vq, lens, bits, out=out, stream=st)
+
+    with torch.cuda.stream(stream):
+        launch_all(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        launch_all(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t_ms = e0.elapsed_time(e1)
+    with torch.cuda.stream(stream):
+        while time.time() - t0 < 1.5:
+            for _ in range(50):
+                graph.replay()
+            stream.synchronize()
+    clocks = sampler.stop()
+    t_max_s = reduce_max(t_ms / 1e3, world)
+    value = aggregate(step_bytes * args.steps / 1e9, world, t_max_s)
+    achieved = step_bytes / (t_ms / 1e3 / args.steps) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        # the fp64 oracle on 2 of the 32 sequences of each cache, scaled to the step
+        t_cpu = 0.0
+        for bits, kq, vq, _ in caches:
+            kc, ks, kz = (t[:2].cpu().numpy() for t in kq)
+            vc, vs, vz = (t[:2].cpu().numpy() for t in vq)
+            Kd = kv_oracle.dequantize(kc, ks.view(np.float16), kz, bits)
+            Vd = kv_oracle.dequantize(vc, vs.view(np.float16), vz, bits)
+            q2 = Q[:2].float().cpu().numpy().astype(np.float64)
+            ts = time.perf_counter()
+            kv_oracle.decode_attention(q2, Kd, Vd, np.full(2, L))
+            t_cpu += time.perf_counter() - ts
+        t_full = t_cpu * Bsz / 2
+        cpu = {"value": round(step_bytes / 1e9 / t_full, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"2 of 32 sequences of each cache (fp64 attention on the dequantised cache, numpy), "
+                         f"{t_cpu:.1f} s measured, scaled by 16 to the step ({t_full:.1f} s)"}
+    out = {
+        "metric": "low-bit KV decode attention GB/s, Llama-3-8B heads (32q/8kv, D=128), 32 seqs x 4096 tokens, "
+                  "int8 + int4 caches",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "kv: decode attention, B=32, L=4096, Hq=32, Hkv=8, D=128, int8 and int4",
+                   "launches_per_step": 2, "bytes_per_step": step_bytes,
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e6:.0f} MB of cache per step)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "peak_source": peaks["source"], "kernel": "kv_attn_kernel"},
+        "gpu_launches": 2 * args.steps, "clocks": clocks, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_rtn_reference(args, rank):
     """Reference arm of --workload rtn: the binary32 oracle on the host."""
     if rank != 0:
@@ -770,7 +871,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu"], default="decode")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu", "kv"], default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
@@ -789,7 +890,7 @@ def main(argv=None):
     if args.impl == "reference":
         if args.workload == "rtn":
             run_rtn_reference(args, rank)
-        elif args.workload == "silu":
+        elif args.workload in ("silu", "kv"):
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the silu workload's reference arm is the "
                                   "oracle timed by the default decode workload"}), flush=True)
@@ -806,6 +907,8 @@ def main(argv=None):
             run_rtn(args, rank, world, local)
         elif args.workload == "silu":
             run_silu(args, rank, world, local)
+        elif args.workload == "kv":
+            run_kv(args, rank, world, local)
         else:
             run_gpu(args, rank, world, local)
     finally:

@@ -104,6 +104,44 @@ tm_status tm_packed_info(const tm_packed* p, int* K, int* N, int* g, size_t* byt
 tm_status tm_quantize_rtn(const uint16_t* W, int K, int N, int g, uint8_t* q, uint8_t* z, uint16_t* s,
                           void* stream);
 
+/*
+ * Low-bit KV cache ("LMDeploy, in depth", section "Quantization: AWQ weights
+ * and KV cache": int8 / int4 keys and values, quantised online,
+ * asymmetrically, per head and per token).
+ *
+ * tm_kv_quantize: `rows` vectors of D fp16 values (one per (token, head),
+ * D = 64, 128 or 256) -> codes, an fp16 scale and a uint8 zero per vector, by
+ * the rule of tm_quantize_rtn with B = 2^bits - 1 in place of 15:
+ *   lo = min(0, min x), hi = max(0, max x); r = hi - lo, or B if r == 0;
+ *   s = fp16(r / B) (>= 2^-24); z = clamp(rint(-lo / s), 0, B); i = 1 / s;
+ *   q = clamp(rint(x * i) + z, 0, B)          (IEEE binary32, ties to even)
+ *   X     : device fp16 [rows][D], 4-byte aligned
+ *   codes : device uint8 [rows][D] (bits 8) or [rows][D/2] (bits 4, even
+ *           index in the low nibble); s: fp16 [rows]; z: uint8 [rows]
+ * Asynchronous on `stream`, one launch.
+ */
+tm_status tm_kv_quantize(const uint16_t* X, long long rows, int D, int bits, uint8_t* codes, uint16_t* s,
+                         uint8_t* z, void* stream);
+
+/*
+ * Decode attention over a quantised KV cache, one query token per sequence:
+ *   out[b][h] = sum_t p_t v~_t,  p = softmax_t(q[b][h] . k~_t / sqrt(D)),
+ *   t < lengths[b], k~ = (qk - zk) sk, v~ = (qv - zv) sv, KV head h / (Hq/Hkv).
+ *   Q      : device fp16 [B][Hq][D], D = 128;   out: device fp16 [B][Hq][D]
+ *   kc, vc : device codes [B][L][Hkv][D*bits/8] (16-byte aligned for int8,
+ *            8 for int4); ks, vs fp16 and kz, vz uint8: [B][L][Hkv]
+ *   lengths: device int32 [B] (clamped to 0..L; 0 gives a zero output)
+ *   split  : CTAs per (sequence, KV head) along the tokens (a cluster, 1..8,
+ *            power of two; 0 = automatic); partial softmax states combine
+ *            through distributed shared memory, no global workspace.
+ * Hq / Hkv must be 1, 2 or 4 (TM_ERR_UNSUPPORTED otherwise).  fp32 softmax
+ * and accumulation.  Asynchronous on `stream`, one launch.
+ */
+tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc, const uint16_t* ks, const uint8_t* kz,
+                                 const uint8_t* vc, const uint16_t* vs, const uint8_t* vz, const int* lengths,
+                                 int B, int Hq, int Hkv, int L, int D, int bits, int split, uint16_t* out,
+                                 void* stream);
+
 /* Release a handle and its device memory (NULL is ignored). */
 void tm_packed_free(tm_packed* p);
 

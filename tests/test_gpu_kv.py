@@ -1,0 +1,120 @@
+"""GPU parity of the low-bit KV cache: the quantiser bit-exact against the
+binary32 oracle; decode attention over an oracle-quantised cache within
+max|out - out_ref| / max|out_ref| <= 2e-3 of the fp64 oracle (fp32 dot products
+over 128 dimensions and an fp32 online softmax contribute ~1e-5; the fp16
+output rounding 2^-11 of |out| dominates)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.kv as kv
+from w4a16_quantized_gemm_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+TOL = 2e-3
+
+
+def _fp16(tag, *shape, scale=1.0):
+    n = int(np.prod(shape))
+    return (synth.normal64(tag, 1, n).reshape(shape) * scale).astype(np.float16)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_kv_quantize_bit_exact(bits, D):
+    X = _fp16(f"kvq/{bits}/{D}", 2, 37, 8, D, scale=0.8)
+    X[0, 0, 0] = 0                       # an all-zero vector
+    X[0, 0, 1] = np.float16(0.3)         # a constant vector
+    c, s, z = binding.kv_quantize(_dev(X.view(np.uint16)).view(torch.float16), bits)
+    torch.cuda.synchronize()
+    c0, s0, z0 = kv.quantize(X, bits)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), s0.view(np.uint16))
+    assert np.array_equal(z.cpu().numpy(), z0)
+    assert np.array_equal(c.cpu().numpy(), c0)
+
+
+def _cache(B, L, Hkv, bits, tag):
+    K = _fp16(f"{tag}/K", B, L, Hkv, 128)
+    V = _fp16(f"{tag}/V", B, L, Hkv, 128)
+    return kv.quantize(K, bits), kv.quantize(V, bits)
+
+
+def _run(B, L, Hq, Hkv, bits, lengths, split=0, tag="attn"):
+    (kc, ks, kz), (vc, vs, vz) = _cache(B, L, Hkv, bits, f"{tag}/{B}/{L}/{Hkv}/{bits}")
+    Q = _fp16(f"{tag}/Q/{B}/{Hq}", B, Hq, 128)
+    lens = np.asarray(lengths, dtype=np.int32)
+    out = binding.kv_decode_attention(
+        _dev(Q.view(np.uint16)).view(torch.float16),
+        (_dev(kc), _dev(ks.view(np.uint16)).view(torch.float16), _dev(kz)),
+        (_dev(vc), _dev(vs.view(np.uint16)).view(torch.float16), _dev(vz)),
+        _dev(lens), bits, split)
+    torch.cuda.synchronize()
+    ref = kv.decode_attention(Q.astype(np.float64), kv.dequantize(kc, ks, kz, bits), kv.dequantize(vc, vs, vz, bits),
+                              np.minimum(np.maximum(lens, 0), L))
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    return oracle.rel_max_err(got, ref), got, ref
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (16, 8), (8, 8)])
+def test_attention_llama_heads(bits, Hq, Hkv):
+    err, _, _ = _run(2, 1024, Hq, Hkv, bits, [1024, 777])
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_attention_split_override(split, bits):
+    err, _, _ = _run(1, 4096, 32, 8, bits, [4096], split=split)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("L,lengths", [(1, [1]), (37, [37, 5, 16]), (300, [0, 300, 17]), (129, [129, 128, 1])])
+def test_attention_ragged_lengths(L, lengths):
+    err, got, _ = _run(len(lengths), L, 32, 8, 8, lengths)
+    assert err <= TOL, err
+    for b, n in enumerate(lengths):
+        if n == 0:
+            assert np.all(got[b] == 0)
+
+
+def test_attention_long_context_auto_split():
+    err, _, _ = _run(1, 32768, 32, 8, 4, [32768])
+    assert err <= TOL, err
+
+
+def test_quantize_then_attention_pipeline():
+    """GPU quantiser output fed to GPU attention equals the oracle pipeline."""
+    B, L, Hq, Hkv, bits = 2, 513, 32, 8, 8
+    K = _fp16("pipe/K", B, L, Hkv, 128)
+    V = _fp16("pipe/V", B, L, Hkv, 128)
+    Q = _fp16("pipe/Q", B, Hq, 128)
+    kq = binding.kv_quantize(_dev(K.view(np.uint16)).view(torch.float16), bits)
+    vq = binding.kv_quantize(_dev(V.view(np.uint16)).view(torch.float16), bits)
+    lens = np.array([513, 300], dtype=np.int32)
+    out = binding.kv_decode_attention(_dev(Q.view(np.uint16)).view(torch.float16), kq, vq, _dev(lens), bits)
+    torch.cuda.synchronize()
+    k0, v0 = kv.quantize(K, bits), kv.quantize(V, bits)
+    ref = kv.decode_attention(Q.astype(np.float64), kv.dequantize(*k0, bits), kv.dequantize(*v0, bits), lens)
+    assert oracle.rel_max_err(out.float().cpu().numpy().astype(np.float64), ref) <= TOL
+
+
+def test_attention_rejects_unsupported():
+    Q = torch.zeros((1, 24, 128), dtype=torch.float16, device="cuda")
+    c = torch.zeros((1, 4, 3, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 4, 3), dtype=torch.float16, device="cuda")
+    z = torch.zeros((1, 4, 3), dtype=torch.uint8, device="cuda")
+    lens = torch.tensor([4], dtype=torch.int32, device="cuda")
+    with pytest.raises(binding.TMError) as e:       # 8 query heads per KV head
+        binding.kv_decode_attention(Q, (c, s, z), (c, s, z), lens, 8)
+    assert e.value.status == 3

@@ -20,7 +20,8 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
-           "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout")
+           "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
+           "tm_kv_quantize", "tm_kv_decode_attention")
 
 
 class TMError(RuntimeError):
@@ -78,6 +79,10 @@ def load(path: Optional[str] = None):
     lib.tm_device_error.argtypes = [ci, ctypes.POINTER(ctypes.c_uint32)]
     lib.tm_last_launch_count.restype = ci
     lib.tm_last_launch_count.argtypes = []
+    lib.tm_kv_quantize.restype = ci
+    lib.tm_kv_quantize.argtypes = [vp, ctypes.c_longlong, ci, ci, vp, vp, vp, vp]
+    lib.tm_kv_decode_attention.restype = ci
+    lib.tm_kv_decode_attention.argtypes = [vp] * 8 + [ci] * 7 + [vp, vp]
     lib.tm_selftest_wait_timeout.restype = ci
     lib.tm_selftest_wait_timeout.argtypes = [vp]
     lib.tm_w4a16_gemm_silu_mul.restype = ci
@@ -261,6 +266,43 @@ def quantize_rtn(W: torch.Tensor, g: int, stream: Optional[torch.cuda.Stream] = 
         _check(load().tm_quantize_rtn(Wd.data_ptr(), K, N, g, q.data_ptr(), z.data_ptr(), s.data_ptr(),
                                       ctypes.c_void_p(st.cuda_stream)), "tm_quantize_rtn")
     return q, z, s
+
+
+def kv_quantize(X: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] = None):
+    """Quantise fp16 vectors X [..., D] (one per (token, head)) to int8 / int4:
+    returns (codes uint8 [..., D or D/2], s fp16 [...], z uint8 [...])."""
+    if X.dtype != torch.float16 or not X.is_cuda or X.dim() < 1:
+        raise ValueError("X must be a CUDA fp16 tensor [..., D]")
+    X = X.contiguous()
+    D = X.shape[-1]
+    lead = tuple(X.shape[:-1])
+    rows = X.numel() // D if D else 0
+    codes = torch.empty(lead + (D if bits == 8 else D // 2,), dtype=torch.uint8, device=X.device)
+    s = torch.empty(lead, dtype=torch.float16, device=X.device)
+    z = torch.empty(lead, dtype=torch.uint8, device=X.device)
+    st = stream if stream is not None else torch.cuda.current_stream(X.device)
+    _check(load().tm_kv_quantize(X.data_ptr(), rows, D, bits, codes.data_ptr(), s.data_ptr(), z.data_ptr(),
+                                 ctypes.c_void_p(st.cuda_stream)), "tm_kv_quantize")
+    return codes, s, z
+
+
+def kv_decode_attention(Q: torch.Tensor, k: tuple, v: tuple, lengths: torch.Tensor, bits: int, split: int = 0,
+                        out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Q fp16 [B][Hq][D]; k, v = (codes [B][L][Hkv][D*bits/8], s fp16 [B][L][Hkv],
+    z uint8 [B][L][Hkv]); lengths int32 [B].  Returns fp16 [B][Hq][D]."""
+    B, Hq, D = Q.shape
+    kc, ks, kz = k
+    vc, vs, vz = v
+    L, Hkv = kc.shape[1], kc.shape[2]
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float16, device=Q.device)
+    ts = [Q, kc, ks, kz, vc, vs, vz, lengths]
+    if any((not t.is_cuda) or (not t.is_contiguous()) for t in ts) or lengths.dtype != torch.int32:
+        raise ValueError("all inputs must be contiguous CUDA tensors; lengths int32")
+    st = stream if stream is not None else torch.cuda.current_stream(Q.device)
+    _check(load().tm_kv_decode_attention(*(t.data_ptr() for t in ts), B, Hq, Hkv, L, D, bits, split,
+                                         out.data_ptr(), ctypes.c_void_p(st.cuda_stream)), "tm_kv_decode_attention")
+    return out
 
 
 def selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None) -> None:
