@@ -124,18 +124,33 @@ tm_status tm_kv_quantize(const uint16_t* X, long long rows, int D, int bits, uin
                          uint8_t* z, void* stream);
 
 /*
- * Decode attention over a quantised KV cache, one query token per sequence:
+ * Value codes from the token-major layout tm_kv_quantize writes,
+ * [B][L][Hkv][D*bits/8] with D = 128, to the dimension-major 16-token tiles
+ * tm_kv_decode_attention reads: [B][Hkv][L/16][128][16] bytes (int8) or
+ * [B][Hkv][L/16][128][8] (int4, tokens 2k, 2k+1 in the low, high nibble of
+ * byte k).  L % 16 == 0; tiles 16-byte (int8) or 8-byte (int4) aligned.
+ * Asynchronous on `stream`, one launch.
+ */
+tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, uint8_t* tiles, void* stream);
+
+/*
+ * Decode attention over a quantised KV cache, one query token per sequence,
+ * on tensor cores (mma.m16n8k16 on the codes as exact fp16 integers):
  *   out[b][h] = sum_t p_t v~_t,  p = softmax_t(q[b][h] . k~_t / sqrt(D)),
  *   t < lengths[b], k~ = (qk - zk) sk, v~ = (qv - zv) sv, KV head h / (Hq/Hkv).
- *   Q      : device fp16 [B][Hq][D], D = 128;   out: device fp16 [B][Hq][D]
- *   kc, vc : device codes [B][L][Hkv][D*bits/8] (16-byte aligned for int8,
- *            8 for int4); ks, vs fp16 and kz, vz uint8: [B][L][Hkv]
+ *   Q      : device fp16 [B][Hq][D], D = 128, 8-byte aligned; out: fp16 [B][Hq][D]
+ *   kc     : key codes [B][L][Hkv][D*bits/8] (16-byte aligned for int8, 8 for int4)
+ *   vc     : value codes as tiles from tm_kv_pack_v
+ *   ks, vs : fp16 and kz, vz uint8 per (token, head): [B][L][Hkv]
+ *   L      : cache capacity in tokens, a multiple of 16
  *   lengths: device int32 [B] (clamped to 0..L; 0 gives a zero output)
- *   split  : CTAs per (sequence, KV head) along the tokens (a cluster, 1..8,
- *            power of two; 0 = automatic); partial softmax states combine
- *            through distributed shared memory, no global workspace.
- * Hq / Hkv must be 1, 2 or 4 (TM_ERR_UNSUPPORTED otherwise).  fp32 softmax
- * and accumulation.  Asynchronous on `stream`, one launch.
+ *   split  : CTAs per (sequence, KV head) along the tokens (a cluster, 1..8
+ *            (1..4 for 8 query heads per KV head), power of two; 0 =
+ *            automatic); partial softmax states combine through distributed
+ *            shared memory, no global workspace.
+ * Hq / Hkv must be 1, 2, 4 or 8 (TM_ERR_UNSUPPORTED otherwise).  Scores and
+ * softmax in fp32; the value weights p s_v are rounded once to fp16 for the
+ * product.  Asynchronous on `stream`, one launch.
  */
 tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc, const uint16_t* ks, const uint8_t* kz,
                                  const uint8_t* vc, const uint16_t* vs, const uint8_t* vz, const int* lengths,

@@ -21,7 +21,7 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
-           "tm_kv_quantize", "tm_kv_decode_attention")
+           "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v")
 
 
 class TMError(RuntimeError):
@@ -81,6 +81,8 @@ def load(path: Optional[str] = None):
     lib.tm_last_launch_count.argtypes = []
     lib.tm_kv_quantize.restype = ci
     lib.tm_kv_quantize.argtypes = [vp, ctypes.c_longlong, ci, ci, vp, vp, vp, vp]
+    lib.tm_kv_pack_v.restype = ci
+    lib.tm_kv_pack_v.argtypes = [vp, ci, ci, ci, ci, vp, vp]
     lib.tm_kv_decode_attention.restype = ci
     lib.tm_kv_decode_attention.argtypes = [vp] * 8 + [ci] * 7 + [vp, vp]
     lib.tm_selftest_wait_timeout.restype = ci
@@ -286,14 +288,29 @@ def kv_quantize(X: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] 
     return codes, s, z
 
 
+def kv_pack_v(codes: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Value codes [B][L][Hkv][D*bits/8] -> the dimension-major 16-token tiles
+    the attention kernel reads (see tm_kv_pack_v)."""
+    B, L, Hkv, _ = codes.shape
+    codes = codes.contiguous()
+    tiles = torch.empty(B * Hkv * L * 128 * bits // 8, dtype=torch.uint8, device=codes.device)
+    st = stream if stream is not None else torch.cuda.current_stream(codes.device)
+    _check(load().tm_kv_pack_v(codes.data_ptr(), B, L, Hkv, bits, tiles.data_ptr(), ctypes.c_void_p(st.cuda_stream)),
+           "tm_kv_pack_v")
+    return tiles
+
+
 def kv_decode_attention(Q: torch.Tensor, k: tuple, v: tuple, lengths: torch.Tensor, bits: int, split: int = 0,
                         out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Q fp16 [B][Hq][D]; k, v = (codes [B][L][Hkv][D*bits/8], s fp16 [B][L][Hkv],
-    z uint8 [B][L][Hkv]); lengths int32 [B].  Returns fp16 [B][Hq][D]."""
+    """Q fp16 [B][Hq][D]; k = (codes [B][L][Hkv][D*bits/8], s fp16 [B][L][Hkv],
+    z uint8 [B][L][Hkv]); v = (tiles from kv_pack_v, s, z as for k); lengths
+    int32 [B].  Returns fp16 [B][Hq][D]."""
     B, Hq, D = Q.shape
     kc, ks, kz = k
     vc, vs, vz = v
     L, Hkv = kc.shape[1], kc.shape[2]
+    if tuple(vs.shape) != tuple(ks.shape):
+        raise ValueError("value scales must be [B][L][Hkv] like the key scales")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float16, device=Q.device)
     ts = [Q, kc, ks, kz, vc, vs, vz, lengths]
