@@ -124,11 +124,14 @@ tm_status tm_kv_quantize(const uint16_t* X, long long rows, int D, int bits, uin
                          uint8_t* z, void* stream);
 
 /*
- * Value codes from the token-major layout tm_kv_quantize writes,
- * [B][L][Hkv][D*bits/8] with D = 128, to the dimension-major 16-token tiles
- * tm_kv_decode_attention reads: [B][Hkv][L/16][128][16] bytes (int8) or
- * [B][Hkv][L/16][128][8] (int4, tokens 2k, 2k+1 in the low, high nibble of
- * byte k).  L % 16 == 0; tiles 16-byte (int8) or 8-byte (int4) aligned.
+ * Value codes of the head-major cache, [B][Hkv][L][D*bits/8] with D = 128 (as
+ * tm_kv_quantize writes them for vectors ordered (sequence, KV head, token)),
+ * to the tiles tm_kv_decode_attention reads: [B][Hkv][L/16][16*D*bits/8],
+ * each 16-token tile in MMA lane order -- 16-byte chunk (c, lane = 4 gr + t)
+ * holds, for the n8 blocks j of chunk c, the codes of dimension 8 j + gr for
+ * tokens 4t .. 4t+3 (int8: 4 chunks of 4 blocks, a byte per token; int4: 2
+ * chunks of 8 blocks, 16 bits per block, tokens 4t, 4t+1 in the low and high
+ * nibble of the first byte).  L % 16 == 0; tiles 16-byte aligned.
  * Asynchronous on `stream`, one launch.
  */
 tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, uint8_t* tiles, void* stream);
@@ -138,10 +141,12 @@ tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, ui
  * on tensor cores (mma.m16n8k16 on the codes as exact fp16 integers):
  *   out[b][h] = sum_t p_t v~_t,  p = softmax_t(q[b][h] . k~_t / sqrt(D)),
  *   t < lengths[b], k~ = (qk - zk) sk, v~ = (qv - zv) sv, KV head h / (Hq/Hkv).
- *   Q      : device fp16 [B][Hq][D], D = 128, 8-byte aligned; out: fp16 [B][Hq][D]
- *   kc     : key codes [B][L][Hkv][D*bits/8] (16-byte aligned for int8, 8 for int4)
+ * The cache is head-major (each KV head's tokens contiguous):
+ *   Q      : device fp16 [B][Hq][D], D = 128; out: fp16 [B][Hq][D]
+ *   kc     : key codes [B][Hkv][L][D*bits/8]
  *   vc     : value codes as tiles from tm_kv_pack_v
- *   ks, vs : fp16 and kz, vz uint8 per (token, head): [B][L][Hkv]
+ *   ks, vs : fp16 and kz, vz uint8 per (token, head): [B][Hkv][L]
+ *   Q, kc, vc, ks, vs, kz, vz 16-byte aligned (TM_ERR_ALIGNMENT otherwise)
  *   L      : cache capacity in tokens, a multiple of 16
  *   lengths: device int32 [B] (clamped to 0..L; 0 gives a zero output)
  *   split  : CTAs per (sequence, KV head) along the tokens (a cluster, 1..8
@@ -150,7 +155,8 @@ tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, ui
  *            shared memory, no global workspace.
  * Hq / Hkv must be 1, 2, 4 or 8 (TM_ERR_UNSUPPORTED otherwise).  Scores and
  * softmax in fp32; the value weights p s_v are rounded once to fp16 for the
- * product.  Asynchronous on `stream`, one launch.
+ * product.  Waits are bounded: a copy that never lands sets the device
+ * timeout bit (tm_device_error).  Asynchronous on `stream`, one launch.
  */
 tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc, const uint16_t* ks, const uint8_t* kz,
                                  const uint8_t* vc, const uint16_t* vs, const uint8_t* vz, const int* lengths,

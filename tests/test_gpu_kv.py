@@ -43,21 +43,31 @@ def test_kv_quantize_bit_exact(bits, D):
     assert np.array_equal(c.cpu().numpy(), c0)
 
 
+def _hm(a):
+    """[B][L][Hkv](...) -> the head-major cache order [B][Hkv][L](...)."""
+    return np.ascontiguousarray(np.swapaxes(a, 1, 2))
+
+
 def _cache(B, L, Hkv, bits, tag):
     K = _fp16(f"{tag}/K", B, L, Hkv, 128)
     V = _fp16(f"{tag}/V", B, L, Hkv, 128)
     return kv.quantize(K, bits), kv.quantize(V, bits)
 
 
-def _run(B, L, Hq, Hkv, bits, lengths, split=0, tag="attn"):
+def _run(B, L, Hq, Hkv, bits, lengths, split=0, tag="attn", poison_tail=False):
     L = (L + 15) // 16 * 16  # the cache capacity is whole 16-token tiles; lengths stay ragged
     (kc, ks, kz), (vc, vs, vz) = _cache(B, L, Hkv, bits, f"{tag}/{B}/{L}/{Hkv}/{bits}")
     Q = _fp16(f"{tag}/Q/{B}/{Hq}", B, Hq, 128)
     lens = np.asarray(lengths, dtype=np.int32)
+    ks_d, vs_d = ks.copy(), vs.copy()
+    if poison_tail:  # slots past each length hold NaN scales: they must not reach the output
+        for b, n in enumerate(lens):
+            ks_d[b, max(n, 0):] = np.float16(np.nan)
+            vs_d[b, max(n, 0):] = np.float16(np.inf)
     out = binding.kv_decode_attention(
         _dev(Q.view(np.uint16)).view(torch.float16),
-        (_dev(kc), _dev(ks.view(np.uint16)).view(torch.float16), _dev(kz)),
-        (binding.kv_pack_v(_dev(vc), bits), _dev(vs.view(np.uint16)).view(torch.float16), _dev(vz)),
+        (_dev(_hm(kc)), _dev(_hm(ks_d).view(np.uint16)).view(torch.float16), _dev(_hm(kz))),
+        (binding.kv_pack_v(_dev(_hm(vc)), bits), _dev(_hm(vs_d).view(np.uint16)).view(torch.float16), _dev(_hm(vz))),
         _dev(lens), bits, split)
     torch.cuda.synchronize()
     ref = kv.decode_attention(Q.astype(np.float64), kv.dequantize(kc, ks, kz, bits), kv.dequantize(vc, vs, vz, bits),
@@ -81,7 +91,7 @@ def test_attention_split_override(split, bits):
     assert err <= TOL, err
 
 
-@pytest.mark.parametrize("split", [1, 4])
+@pytest.mark.parametrize("split", [1, 4, 8])
 def test_attention_eight_heads_per_kv_head(split):
     err, _, _ = _run(2, 512, 64, 8, 8, [512, 100], split=split)
     assert err <= TOL, err
@@ -96,6 +106,12 @@ def test_attention_ragged_lengths(L, lengths):
             assert np.all(got[b] == 0)
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_attention_ignores_the_cache_past_each_length(bits):
+    err, _, _ = _run(3, 400, 32, 8, bits, [400, 131, 7], poison_tail=True)
+    assert err <= TOL, err
+
+
 def test_attention_long_context_auto_split():
     err, _, _ = _run(1, 32768, 32, 8, 4, [32768])
     assert err <= TOL, err
@@ -107,8 +123,8 @@ def test_quantize_then_attention_pipeline():
     K = _fp16("pipe/K", B, L, Hkv, 128)
     V = _fp16("pipe/V", B, L, Hkv, 128)
     Q = _fp16("pipe/Q", B, Hq, 128)
-    kq = binding.kv_quantize(_dev(K.view(np.uint16)).view(torch.float16), bits)
-    vq = binding.kv_quantize(_dev(V.view(np.uint16)).view(torch.float16), bits)
+    kq = binding.kv_quantize(_dev(_hm(K).view(np.uint16)).view(torch.float16), bits)
+    vq = binding.kv_quantize(_dev(_hm(V).view(np.uint16)).view(torch.float16), bits)
     lens = np.array([513, 300], dtype=np.int32)
     vq = (binding.kv_pack_v(vq[0], bits), vq[1], vq[2])
     out = binding.kv_decode_attention(_dev(Q.view(np.uint16)).view(torch.float16), kq, vq, _dev(lens), bits)
@@ -120,16 +136,28 @@ def test_quantize_then_attention_pipeline():
 
 def test_attention_rejects_unsupported():
     Q = torch.zeros((1, 48, 128), dtype=torch.float16, device="cuda")
-    c = torch.zeros((1, 16, 3, 128), dtype=torch.uint8, device="cuda")
-    s = torch.zeros((1, 16, 3), dtype=torch.float16, device="cuda")
-    z = torch.zeros((1, 16, 3), dtype=torch.uint8, device="cuda")
+    c = torch.zeros((1, 3, 16, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 3, 16), dtype=torch.float16, device="cuda")
+    z = torch.zeros((1, 3, 16), dtype=torch.uint8, device="cuda")
     lens = torch.tensor([4], dtype=torch.int32, device="cuda")
     with pytest.raises(binding.TMError) as e:       # 16 query heads per KV head
         binding.kv_decode_attention(Q, (c, s, z), (c, s, z), lens, 8)
     assert e.value.status == 3
-    c = torch.zeros((1, 12, 3, 128), dtype=torch.uint8, device="cuda")
-    s = torch.zeros((1, 12, 3), dtype=torch.float16, device="cuda")
-    z = torch.zeros((1, 12, 3), dtype=torch.uint8, device="cuda")
+    c = torch.zeros((1, 3, 12, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 3, 12), dtype=torch.float16, device="cuda")
+    z = torch.zeros((1, 3, 12), dtype=torch.uint8, device="cuda")
     with pytest.raises(binding.TMError) as e:       # capacity not a multiple of 16 tokens
         binding.kv_decode_attention(Q[:, :6], (c, s, z), (c, s, z), lens, 8)
     assert e.value.status == 1
+
+
+def test_attention_rejects_misaligned_cache():
+    Q = torch.zeros((1, 8, 128), dtype=torch.float16, device="cuda")
+    c = torch.zeros((1, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((1, 2, 16), dtype=torch.float16, device="cuda")
+    z = torch.zeros((1, 2, 16), dtype=torch.uint8, device="cuda")
+    z_off = torch.zeros(2 * 16 + 1, dtype=torch.uint8, device="cuda")[1:].view(1, 2, 16)  # one byte off
+    lens = torch.tensor([4], dtype=torch.int32, device="cuda")
+    with pytest.raises(binding.TMError) as e:
+        binding.kv_decode_attention(Q, (c, s, z_off), (c, s, z), lens, 8)
+    assert e.value.status == 2

@@ -289,9 +289,9 @@ def kv_quantize(X: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] 
 
 
 def kv_pack_v(codes: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Value codes [B][L][Hkv][D*bits/8] -> the dimension-major 16-token tiles
-    the attention kernel reads (see tm_kv_pack_v)."""
-    B, L, Hkv, _ = codes.shape
+    """Value codes [B][Hkv][L][D*bits/8] -> the 16-token tiles in MMA lane
+    order the attention kernel reads (see tm_kv_pack_v)."""
+    B, Hkv, L, _ = codes.shape
     codes = codes.contiguous()
     tiles = torch.empty(B * Hkv * L * 128 * bits // 8, dtype=torch.uint8, device=codes.device)
     st = stream if stream is not None else torch.cuda.current_stream(codes.device)
@@ -302,15 +302,15 @@ def kv_pack_v(codes: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream
 
 def kv_decode_attention(Q: torch.Tensor, k: tuple, v: tuple, lengths: torch.Tensor, bits: int, split: int = 0,
                         out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Q fp16 [B][Hq][D]; k = (codes [B][L][Hkv][D*bits/8], s fp16 [B][L][Hkv],
-    z uint8 [B][L][Hkv]); v = (tiles from kv_pack_v, s, z as for k); lengths
-    int32 [B].  Returns fp16 [B][Hq][D]."""
+    """Q fp16 [B][Hq][D]; k = (codes [B][Hkv][L][D*bits/8], s fp16 [B][Hkv][L],
+    z uint8 [B][Hkv][L]) -- the head-major cache; v = (tiles from kv_pack_v,
+    s, z as for k); lengths int32 [B].  Returns fp16 [B][Hq][D]."""
     B, Hq, D = Q.shape
     kc, ks, kz = k
     vc, vs, vz = v
-    L, Hkv = kc.shape[1], kc.shape[2]
-    if tuple(vs.shape) != tuple(ks.shape):
-        raise ValueError("value scales must be [B][L][Hkv] like the key scales")
+    Hkv, L = kc.shape[1], kc.shape[2]
+    if tuple(ks.shape) != (B, Hkv, L) or tuple(vs.shape) != (B, Hkv, L):
+        raise ValueError("scales and zeros must be [B][Hkv][L] like the key codes")
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float16, device=Q.device)
     ts = [Q, kc, ks, kz, vc, vs, vz, lengths]

@@ -17,16 +17,24 @@
 //   s = fp16(r / B), at least 2^-24;  z = clamp(rint(-lo / s), 0, B)
 //   i = 1 / s;  q = clamp(rint(x * i) + z, 0, B)
 // Codes: one byte each (int8) or two per byte, even index in the low nibble
-// (int4); s fp16 and z uint8 per (token, head).  Keys stay token-major; values
-// are re-laid dimension-major in 16-token tiles (tm_kv_pack_v) for the P V
-// product.
+// (int4); s fp16 and z uint8 per (token, head).
+//
+// Cache layout (ours; the pages' paged cache keeps each KV head's tokens
+// together inside a block): head-major, so that the 16-token tiles of one
+// (sequence, KV head) are contiguous --
+//   key codes   [B][Hkv][L][D * bits / 8]   (as tm_kv_quantize writes them)
+//   value codes [B][Hkv][L / 16][tile]      (tm_kv_pack_v re-lays each tile in
+//                                           the MMA lane order)
+//   ks, kz, vs, vz [B][Hkv][L]
 //
 // Attention, one query token per sequence, D = 128, G = Hq / Hkv query heads
-// per KV head: a CTA takes one (sequence, KV head) and a slice of its tokens,
-// a warp a 16-token tile at a time with an online softmax per head; the warps'
-// states combine in shared memory, then over the CTAs of a thread-block
-// cluster through distributed shared memory (no global scratch), and rank 0
-// writes the output.
+// per KV head: a CTA takes one (sequence, KV head) and a slice of its tokens;
+// a producer warp streams them through a ring of shared-memory slots of 128
+// tokens (bulk copies completing on mbarriers), and each of 8 consumer warps
+// takes one 16-token tile of every slot and keeps an online softmax per head;
+// the warps' states combine in shared memory, then over the CTAs of a
+// thread-block cluster through distributed shared memory (no global scratch),
+// and rank 0 writes the output.
 #include <math_constants.h>
 
 #include "tm_common.cuh"
@@ -91,59 +99,92 @@ __global__ void __launch_bounds__(128) kv_quant_kernel(const __half* __restrict_
   }
 }
 
+
 // ------------------------------------------------------------ attention -----
 
 constexpr int kAttnD = 128;
-constexpr int kAttnThreads = 128;  // 4 warps, a 16-token tile each at a time
-constexpr int kWarps = kAttnThreads / 32;
-// CTAs per cluster along the tokens; the combine buffer holds one state per CTA
-// and must stay within the 48 KB of static shared memory.
-__host__ __device__ constexpr int max_split(int G) { return G == 8 ? 4 : 8; }
+constexpr int kConsumers = 8;                    // warps that compute, one 16-token tile of a slot each
+constexpr int kAttnThreads = 32 * (kConsumers + 1);  // + one producer warp
+constexpr int kSlotTiles = kConsumers;           // 16-token tiles per ring slot
+constexpr int kState = 2 + kAttnD;               // max, sum, 128 accumulators per query head
+constexpr int kMaxSplit = 8;                     // CTAs per cluster along the tokens
+
+__device__ uint32_t s_err_kv;
+
+// One ring slot holds 8 consecutive 16-token tiles of one (sequence, KV
+// head): key codes (rows of D * BITS / 8 bytes), value tiles, then ks, vs
+// (fp16) and kz, vz (uint8) per token; each region sized for 8 tiles and
+// filled from its start (the last slot of a CTA may hold fewer tiles).
+template <int BITS>
+struct KvSlot {
+  static constexpr uint32_t kTile = 16 * kAttnD * BITS / 8;  // code bytes of one tile
+  static constexpr uint32_t kK = 0, kV = kSlotTiles * kTile, kKs = 2 * kSlotTiles * kTile;
+  static constexpr uint32_t kVs = kKs + 32 * kSlotTiles, kKz = kVs + 32 * kSlotTiles, kVz = kKz + 16 * kSlotTiles;
+  static constexpr uint32_t kBytes = kVz + 16 * kSlotTiles;
+  static constexpr int kDepth = BITS == 8 ? 3 : 6;  // ~100 KB: two CTAs per SM
+  static constexpr uint32_t kRing = kDepth * kBytes;
+  static constexpr uint32_t kCombine = (uint32_t)(kConsumers + kMaxSplit) * 8 * kState * 4;  // G <= 8
+  static constexpr uint32_t kBarOff = kRing > kCombine ? kRing : kCombine;
+  static constexpr uint32_t kSmem = kBarOff + 16 * kDepth + 16;  // full, empty barriers; abort flag
+};
 
 struct AttnParams {
-  const __half* Q;        // [B][Hq][D]
-  const uint8_t* kc;      // [B][L][Hkv][D * BITS / 8]
-  const __half* ks;       // [B][L][Hkv]
-  const uint8_t* kz;
-  const uint8_t* vc;
+  const __half* Q;     // [B][Hq][D]
+  const uint8_t* kc;   // [B][Hkv][L][D * BITS / 8]
+  const __half* ks;    // [B][Hkv][L]
+  const uint8_t* kz;   // [B][Hkv][L]
+  const uint8_t* vc;   // [B][Hkv][L / 16][16 * D * BITS / 8], lane order (tm_kv_pack_v)
   const __half* vs;
   const uint8_t* vz;
-  const int* lengths;     // [B]
-  __half* out;            // [B][Hq][D]
+  const int* lengths;  // [B]
+  __half* out;         // [B][Hq][D]
   int L, Hq, Hkv;
 };
 
-// Combine the per-warp softmax states in `part` (max, sum, 128-dim accumulator
-// per query head) into one per CTA, then over the CTAs of the cluster through
-// distributed shared memory into rank 0, which writes out = acc / sum.
+__device__ __forceinline__ bool kv_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(&s_err_kv, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Combine the per-warp softmax states part[w][h][.] into one per CTA, then
+// over the CTAs of the cluster through distributed shared memory into rank
+// 0's cta[r][h][.], which writes out = acc / sum.
 template <int G>
-__device__ __forceinline__ void finish_attention(float (*part)[G][2 + kAttnD], float (*cta)[G][2 + kAttnD],
-                                                 const AttnParams& P, int b, int kvh, int S, int rank) {
+__device__ __forceinline__ void finish_attention(const float* part, float* cta, const AttnParams& P, int b, int kvh,
+                                                 int S, int rank) {
   __syncthreads();
-  // thread -> (head, dimension): G x 128 outputs over 128 threads
-  float* dst_local = &cta[0][0][0];
-  const uint32_t cta_base = smem_u32(dst_local);
-  if (S > 1) cluster_sync_all();  // every CTA of the cluster is running before remote stores
-  for (int e = threadIdx.x; e < G * (2 + kAttnD); e += kAttnThreads) {
-    const int h = e / (2 + kAttnD), k = e % (2 + kAttnD);
+  if (S > 1) cluster_sync_all();  // every CTA of the cluster is past its loop before remote stores
+  const uint32_t cta_base = smem_u32(cta);
+  for (int e = threadIdx.x; e < G * kState; e += kAttnThreads) {
+    const int h = e / kState, k = e % kState;
     float mx = -CUDART_INF_F;
 #pragma unroll
-    for (int s2 = 0; s2 < kWarps; ++s2) mx = fmaxf(mx, part[s2][h][0]);
+    for (int w = 0; w < kConsumers; ++w) mx = fmaxf(mx, part[(w * G + h) * kState]);
     float v = 0.f;
     if (k == 0) {
       v = mx;
     } else {
 #pragma unroll
-      for (int s2 = 0; s2 < kWarps; ++s2) {
-        const float w = part[s2][h][0] == -CUDART_INF_F ? 0.f : expf(part[s2][h][0] - mx);
-        v = fmaf(part[s2][h][k], w, v);
+      for (int w = 0; w < kConsumers; ++w) {
+        const float m = part[(w * G + h) * kState];
+        const float s = m == -CUDART_INF_F ? 0.f : expf(m - mx);
+        v = fmaf(part[(w * G + h) * kState + k], s, v);
       }
     }
-    const uint32_t off = (uint32_t)(((rank * G + h) * (2 + kAttnD) + k) * 4);
+    const int idx = (rank * G + h) * kState + k;
     if (S > 1) {
-      st_dsmem_f32(map_shared_rank(cta_base + off, 0u), v);
+      st_dsmem_f32(map_shared_rank(cta_base + 4u * idx, 0u), v);
     } else {
-      cta[0][h][k] = v;
+      cta[idx] = v;
     }
   }
   if (S > 1) {
@@ -155,226 +196,387 @@ __device__ __forceinline__ void finish_attention(float (*part)[G][2 + kAttnD], f
   for (int e = threadIdx.x; e < G * kAttnD; e += kAttnThreads) {
     const int h = e / kAttnD, d = e % kAttnD;
     float mx = -CUDART_INF_F;
-    for (int r = 0; r < S; ++r) mx = fmaxf(mx, cta[r][h][0]);
+    for (int r = 0; r < S; ++r) mx = fmaxf(mx, cta[(r * G + h) * kState]);
     float num = 0.f, den = 0.f;
     if (mx != -CUDART_INF_F) {
       for (int r = 0; r < S; ++r) {
-        if (cta[r][h][0] == -CUDART_INF_F) continue;
-        const float w = expf(cta[r][h][0] - mx);
-        den = fmaf(cta[r][h][1], w, den);
-        num = fmaf(cta[r][h][2 + d], w, num);
+        const float m = cta[(r * G + h) * kState];
+        if (m == -CUDART_INF_F) continue;
+        const float w = expf(m - mx);
+        den = fmaf(cta[(r * G + h) * kState + 1], w, den);
+        num = fmaf(cta[(r * G + h) * kState + 2 + d], w, num);
       }
     }
     P.out[((size_t)b * P.Hq + kvh * G + h) * kAttnD + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
   }
 }
 
-
 // ------------------------------------------------ tensor-core attention -----
 //
-// Per warp a tile of 16 tokens.  Scores S^T = Q K^T on mma.m16n8k16: A = the
-// query heads (G of 16 rows used), B = the key codes as exact fp16 integers
-// (the fp16 pattern of 1024 OR-ed with a code, minus 1024), so
-// score = s_k (Q . c - z_k sum Q) / sqrt(D) per token in fp32 afterwards.  The
-// k order inside every 16-dimension slice is permuted the same way on Q and K
-// (slots 2t, 2t+1, 2t+8, 2t+9 hold dimensions 4t .. 4t+3), so a lane reads
-// its key bytes with one 4-byte (int8) or 2-byte (int4) load.  Within the
-// tile, the first n8 block holds tokens {0,1,4,5,8,9,12,13} and the second
-// {2,3,6,7,10,11,14,15}: then the score fragment of a lane (head gr, tokens
-// 4t .. 4t+3) is exactly its A fragment of P for out = P V (tokens 4t .. 4t+3
-// in slots 2t, 2t+1, 2t+8, 2t+9).  P carries the per-token value scale
-// (rounded once to fp16); V codes come from tiles stored dimension-major
-// ([128 dims][16 tokens], written by tm_kv_pack_v), one 4- or 2-byte load per
-// lane and n8 block of dimensions; the value zero point is removed once per
-// head at the end (sum_t P_t z_t).
+// Per consumer warp one 16-token tile of each slot, on mma.m16n8k16 with the
+// tokens and the dimensions as the 16-row side and the (up to 8) query heads
+// of the KV head as the 8 columns, so no accumulator is wasted:
+//   scores^T [16 tokens x 8 heads] = K codes [16 x 128] . Q^T, 8 MMAs: the
+//     codes become exact fp16 integers (the fp16 pattern of 1024 OR-ed with a
+//     code, minus 1024) and score = s_k (Q . c - z_k sum Q) / sqrt(D) per
+//     token afterwards, in fp32.  The k order is permuted the same way on K
+//     and Q: in slice sl the slots 2t, 2t+1, 2t+8, 2t+9 of lane t hold
+//     dimensions 32t + 4sl .. 32t + 4sl + 3, so a lane reads the 32 dimensions
+//     it needs of a token with two (int8) or one (int4) 16-byte loads.
+//   out^T [128 dims x 8 heads] += V codes^T . P', 8 MMAs: P' = p s_v (rounded
+//     once to fp16) is the score fragment transposed by two movmatrix; the
+//     value tile holds, per lane, the codes of dimensions 8q + gr (q = 0..15)
+//     for tokens 2t, 2t+1, 2t+8, 2t+9 in MMA A-fragment order.  The value
+//     zero point is removed once per head at the end (sum_t P'_t z_t).
+// A lane (gr, t) owns query heads 2t and 2t+1 throughout: after the max over
+// the tile's tokens (three shuffles) the online softmax is lane-local.
 
-// Two codes -> two exact fp16 values (int8: bytes i, i+1 of w; int4: both
-// nibbles of byte i of w).
+// Two codes -> two exact fp16 values.  int8: bytes 2i, 2i+1 of w; int4: the
+// low and high nibble of byte i of w.
 template <int BITS>
 __device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, int i) {
   if constexpr (BITS == 8) {
     const uint32_t x = __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);  // (1024 + c0, 1024 + c1)
     return hsub2_u32(x, 0x64006400u);
   } else {
-    const uint32_t x = __byte_perm(w, 0u, i == 0 ? 0x4040u : 0x4141u);       // byte i in bytes 0 and 2
-    const uint32_t y = lop3<0xEA>(x, 0x00F0000Fu, 0x64006400u);              // (1024 + lo, 1024 + 16 hi)
-    return hfma2_u32(y, 0x2C003C00u, 0xD400E400u);                          // (x - 1024, x / 16 - 64)
+    const uint32_t x = __byte_perm(w, 0u, 0x4040u | (uint32_t)i | ((uint32_t)i << 8));  // byte i in bytes 0 and 2
+    const uint32_t y = lop3<0xEA>(x, 0x00F0000Fu, 0x64006400u);  // (1024 + lo, 1024 + 16 hi)
+    return hfma2_u32(y, 0x2C003C00u, 0xD400E400u);              // (x - 1024, x / 16 - 64)
   }
 }
 
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 template <int BITS, int G>
-__global__ void __launch_bounds__(kAttnThreads) kv_attn_tc_kernel(const AttnParams P) {
-  constexpr int RB = kAttnD * BITS / 8;  // key code bytes per (token, head)
-  constexpr int TB = 16 * BITS / 8;      // value tile bytes per dimension (16 tokens)
-  __shared__ float part[kWarps][G][2 + kAttnD];
-  __shared__ float cta[max_split(G)][G][2 + kAttnD];  // rank 0: one state per CTA of the cluster
+__global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
+  using SL = KvSlot<BITS>;
+  constexpr int RB = kAttnD * BITS / 8;  // code bytes per (token, head)
+  constexpr int NS = SL::kDepth;
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t = lane & 3;
-  const int b = blockIdx.x / P.Hkv, kvh = blockIdx.x % P.Hkv;
+  const int bh = blockIdx.x, b = bh / P.Hkv, kvh = bh % P.Hkv;
   const int S = gridDim.y, rank = blockIdx.y;
   const int n = max(0, min(P.lengths[b], P.L));
   const int chunk = ((n + S - 1) / S + 15) & ~15;  // whole 16-token tiles per CTA
   const int t_begin = min(n, rank * chunk), t_end = min(n, t_begin + chunk);
-  const bool head = gr < G;
-
-  // A fragments of Q (rows gr < G), permuted k order; and sum_d Q[gr][d]
-  uint32_t qa[8][2];
-  float qsum = 0.f;
-#pragma unroll
-  for (int sl = 0; sl < 8; ++sl) {
-    uint2 v = make_uint2(0u, 0u);
-    if (head) v = *reinterpret_cast<const uint2*>(P.Q + ((size_t)b * P.Hq + kvh * G + gr) * kAttnD + 16 * sl + 4 * t);
-    qa[sl][0] = v.x;
-    qa[sl][1] = v.y;
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-    qsum += (f0.x + f0.y) + (f1.x + f1.y);
+  const int nslots = (t_end - t_begin + 16 * kSlotTiles - 1) / (16 * kSlotTiles);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + SL::kBarOff, bar_empty = bar_full + 8 * NS;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kBarOff + 16 * NS);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumers);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-  qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+  __syncthreads();
+
+  float* part = reinterpret_cast<float*>(smem);  // overlays the ring after the loop
+  float* cta = part + kConsumers * G * kState;
+
+  if (warp == kConsumers) {
+    // ---- producer: one lane streams the slots with bulk copies
+    if (lane == 0) {
+      const size_t seq = (size_t)bh * P.L;  // first token of this (sequence, KV head) in [B][Hkv][L]
+      int issued = 0;
+      for (int i = 0; i < nslots; ++i) {
+        const int slot = i % NS;
+        if (i >= NS && !kv_wait(bar_empty + 8 * slot, (uint32_t)(i / NS - 1) & 1u, abort_flag)) break;
+        const int tok0 = t_begin + 16 * kSlotTiles * i;
+        const int tiles = min(kSlotTiles, (t_end - tok0 + 15) / 16);
+        const uint32_t dst = sbase + slot * SL::kBytes, bar = bar_full + 8 * slot;
+        mbar_expect_tx(bar, (uint32_t)tiles * (2 * SL::kTile + 96));
+        bulk_g2s(dst + SL::kK, P.kc + (seq + tok0) * RB, tiles * SL::kTile, bar);
+        bulk_g2s(dst + SL::kV, P.vc + (seq + tok0) * RB, tiles * SL::kTile, bar);
+        bulk_g2s(dst + SL::kKs, P.ks + seq + tok0, tiles * 32, bar);
+        bulk_g2s(dst + SL::kVs, P.vs + seq + tok0, tiles * 32, bar);
+        bulk_g2s(dst + SL::kKz, P.kz + seq + tok0, tiles * 16, bar);
+        bulk_g2s(dst + SL::kVz, P.vz + seq + tok0, tiles * 16, bar);
+        issued = i + 1;
+      }
+      // never leave with copies in flight into this CTA's shared memory
+      for (int k = max(0, issued - NS); k < issued; ++k) {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(bar_full + 8 * (k % NS), (uint32_t)(k / NS) & 1u))
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(&s_err_kv, kErrTimeout);
+            break;
+          }
+      }
+    }
+    __syncwarp();
+    __syncthreads();  // the consumers have written `part`
+    finish_attention<G>(part, cta, P, b, kvh, S, rank);
+    return;
+  }
+
+  // ---- consumers
+  const int gr = lane >> 2, t = lane & 3;
+  // B fragments of Q^T (column gr = query head gr < G) in the permuted k order,
+  // and sum_d Q[h][d] for this lane's heads 2t, 2t+1
+  uint32_t qb[8][2];
+  float qs0, qs1;
+  {
+    uint4 q4[4] = {};
+    if (gr < G) {
+      const uint4* qp = reinterpret_cast<const uint4*>(P.Q + ((size_t)b * P.Hq + kvh * G + gr) * kAttnD + 32 * t);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) q4[c] = qp[c];
+    }
+    float qsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t wv[4] = {q4[c].x, q4[c].y, q4[c].z, q4[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
+        qsum += f.x + f.y;
+      }
+      qb[2 * c][0] = wv[0];
+      qb[2 * c][1] = wv[1];
+      qb[2 * c + 1][0] = wv[2];
+      qb[2 * c + 1][1] = wv[3];
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // head gr
+    qs0 = __shfl_sync(0xffffffffu, qsum, 8 * t);      // head 2t
+    qs1 = __shfl_sync(0xffffffffu, qsum, 8 * t + 4);  // head 2t + 1
+  }
   const float scale = rsqrtf((float)kAttnD);
 
-  float m = -CUDART_INF_F, lp = 0.f, zc = 0.f;  // running max; this lane's partial sums
-  float o[16][4];
+  // heads 2t, 2t+1: running max, and this lane's partial sums of p and p' z
+  float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+  float o[8][4];  // out^T: dims 16p + gr (0, 1) and 16p + 8 + gr (2, 3); heads 2t (0, 2), 2t+1 (1, 3)
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
+  for (int p = 0; p < 8; ++p)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
+    for (int e = 0; e < 4; ++e) o[p][e] = 0.f;
 
-  const size_t tiles_per_seq = (size_t)P.L / 16;
-  for (int t0 = t_begin + 16 * warp; t0 < t_end; t0 += 16 * kWarps) {
-    // ---- scores: two n8 blocks of tokens
-    float r[4];
-#pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
-      const int tok = t0 + 4 * (gr >> 1) + (gr & 1) + 2 * nb;  // this lane's B row (token)
-      const uint8_t* krow = P.kc + (((size_t)b * P.L + tok) * P.Hkv + kvh) * RB;
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = 0; i < nslots; ++i) {
+    const int slot = i % NS;
+    if (!__all_sync(0xffffffffu, kv_wait(bar_full + 8 * slot, (uint32_t)(i / NS) & 1u, abort_flag))) break;
+    const int t0 = t_begin + 16 * (kSlotTiles * i + warp);  // this warp's tile
+    if (t0 < t_end) {
+      const uint8_t* sp = smem + slot * SL::kBytes;
+      // ---- scores^T: rows = tokens gr, gr + 8; columns = heads 2t, 2t + 1
+      uint32_t wa[8], wb[8];  // code words of tokens gr and gr + 8
+      {
+        const uint8_t* ka = sp + SL::kK + (warp * 16 + gr) * RB;
+        const uint8_t* kb = ka + 8 * RB;
+        if constexpr (BITS == 8) {
+          // odd rows read their two halves in the other order: no bank conflict
+          const int h = gr & 1;
+          const uint4 a0 = *reinterpret_cast<const uint4*>(ka + 32 * t + 16 * h);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(ka + 32 * t + 16 * (h ^ 1));
+          const uint4 b0 = *reinterpret_cast<const uint4*>(kb + 32 * t + 16 * h);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(kb + 32 * t + 16 * (h ^ 1));
+          const uint4 alo = h ? a1 : a0, ahi = h ? a0 : a1, blo = h ? b1 : b0, bhi = h ? b0 : b1;
+          wa[0] = alo.x, wa[1] = alo.y, wa[2] = alo.z, wa[3] = alo.w;
+          wa[4] = ahi.x, wa[5] = ahi.y, wa[6] = ahi.z, wa[7] = ahi.w;
+          wb[0] = blo.x, wb[1] = blo.y, wb[2] = blo.z, wb[3] = blo.w;
+          wb[4] = bhi.x, wb[5] = bhi.y, wb[6] = bhi.z, wb[7] = bhi.w;
+        } else {
+          const uint4 a = *reinterpret_cast<const uint4*>(ka + 16 * t);
+          const uint4 c = *reinterpret_cast<const uint4*>(kb + 16 * t);
+          wa[0] = a.x, wa[1] = a.y, wa[2] = a.z, wa[3] = a.w;
+          wb[0] = c.x, wb[1] = c.y, wb[2] = c.z, wb[3] = c.w;
+        }
+      }
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};  // two chains over the slices
 #pragma unroll
       for (int sl = 0; sl < 8; ++sl) {
-        uint32_t w;
+        uint32_t a[4];
         if constexpr (BITS == 8) {
-          w = *reinterpret_cast<const uint32_t*>(krow + 16 * sl + 4 * t);
+          a[0] = codes_to_half2<8>(wa[sl], 0);
+          a[1] = codes_to_half2<8>(wb[sl], 0);
+          a[2] = codes_to_half2<8>(wa[sl], 1);
+          a[3] = codes_to_half2<8>(wb[sl], 1);
         } else {
-          w = *reinterpret_cast<const uint16_t*>(krow + 8 * sl + 2 * t);
+          const int by = 2 * (sl & 1);
+          a[0] = codes_to_half2<4>(wa[sl >> 1], by);
+          a[1] = codes_to_half2<4>(wb[sl >> 1], by);
+          a[2] = codes_to_half2<4>(wa[sl >> 1], by + 1);
+          a[3] = codes_to_half2<4>(wb[sl >> 1], by + 1);
         }
-        const uint32_t a[4] = {qa[sl][0], 0u, qa[sl][1], 0u};
-        mma_16816(d, a, codes_to_half2<BITS>(w, 0), codes_to_half2<BITS>(w, 1));
+        mma_16816((sl & 1) ? d1 : d0, a, qb[sl][0], qb[sl][1]);
       }
-      r[2 * nb] = d[0];      // token 4t + 2 nb
-      r[2 * nb + 1] = d[1];  // token 4t + 2 nb + 1
-    }
-    float sc[4], vsc[4], vzp[4];
-    float mt = -CUDART_INF_F;
+      // per-token scales of tokens gr (index 0) and gr + 8 (index 1)
+      const __half* ksp = reinterpret_cast<const __half*>(sp + SL::kKs) + warp * 16;
+      const __half* vsp = reinterpret_cast<const __half*>(sp + SL::kVs) + warp * 16;
+      const uint8_t* kzp = sp + SL::kKz + warp * 16;
+      const uint8_t* vzp = sp + SL::kVz + warp * 16;
+      const bool va = t0 + gr < t_end, vb = t0 + gr + 8 < t_end;
+      const float ka_s = __half2float(ksp[gr]) * scale, kb_s = __half2float(ksp[gr + 8]) * scale;
+      const float ka_z = (float)kzp[gr], kb_z = (float)kzp[gr + 8];
+      const float s00 = va ? ka_s * fmaf(-ka_z, qs0, d0[0] + d1[0]) : -CUDART_INF_F;  // token gr, head 2t
+      const float s01 = va ? ka_s * fmaf(-ka_z, qs1, d0[1] + d1[1]) : -CUDART_INF_F;  // token gr, head 2t+1
+      const float s10 = vb ? kb_s * fmaf(-kb_z, qs0, d0[2] + d1[2]) : -CUDART_INF_F;  // token gr+8, head 2t
+      const float s11 = vb ? kb_s * fmaf(-kb_z, qs1, d0[3] + d1[3]) : -CUDART_INF_F;  // token gr+8, head 2t+1
+      float mt0 = fmaxf(s00, s10), mt1 = fmaxf(s01, s11);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int tok = t0 + 4 * t + i;
-      if (tok < t_end) {
-        const size_t th = ((size_t)b * P.L + tok) * P.Hkv + kvh;
-        sc[i] = __half2float(P.ks[th]) * fmaf(-(float)P.kz[th], qsum, r[i]) * scale;
-        vsc[i] = __half2float(P.vs[th]);
-        vzp[i] = (float)P.vz[th];
-      } else {
-        sc[i] = -CUDART_INF_F;
-        vsc[i] = 0.f;
-        vzp[i] = 0.f;
+      for (int x = 4; x < 32; x <<= 1) {
+        mt0 = fmaxf(mt0, __shfl_xor_sync(0xffffffffu, mt0, x));
+        mt1 = fmaxf(mt1, __shfl_xor_sync(0xffffffffu, mt1, x));
       }
-      mt = fmaxf(mt, sc[i]);
-    }
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-    const float mn = fmaxf(m, mt);  // finite: every tile holds at least one valid token
-    const float alpha = expf(m - mn);  // 0 on the first tile (m = -inf)
-    m = mn;
-    __half ph[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float p = expf(sc[i] - mn);
-      lp = fmaf(lp, i == 0 ? alpha : 1.f, p);
-      ph[i] = __float2half_rn(p * vsc[i]);
-    }
-    zc = fmaf(zc, alpha, __half2float(ph[0]) * vzp[0] + __half2float(ph[1]) * vzp[1] +
-                             __half2float(ph[2]) * vzp[2] + __half2float(ph[3]) * vzp[3]);
-    const uint32_t pa[4] = {(uint32_t)__half_as_ushort(ph[0]) | ((uint32_t)__half_as_ushort(ph[1]) << 16), 0u,
-                            (uint32_t)__half_as_ushort(ph[2]) | ((uint32_t)__half_as_ushort(ph[3]) << 16), 0u};
-    // ---- out += P V over 16 n8 blocks of dimensions
-    const uint8_t* vt = P.vc + (((size_t)b * P.Hkv + kvh) * tiles_per_seq + t0 / 16) * kAttnD * TB;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      o[j][0] *= alpha;
-      o[j][1] *= alpha;
-      uint32_t w;
-      if constexpr (BITS == 8) {
-        w = *reinterpret_cast<const uint32_t*>(vt + (8 * j + gr) * TB + 4 * t);
-      } else {
-        w = *reinterpret_cast<const uint16_t*>(vt + (8 * j + gr) * TB + 2 * t);
+      const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);  // finite: token t0 is valid
+      const bool rescale = !__all_sync(0xffffffffu, mn0 == m0 && mn1 == m1);
+      const float al0 = expf(m0 - mn0), al1 = expf(m1 - mn1);  // 0 on the first tile
+      m0 = mn0;
+      m1 = mn1;
+      const float p00 = expf(s00 - mn0), p01 = expf(s01 - mn1), p10 = expf(s10 - mn0), p11 = expf(s11 - mn1);
+      l0 = fmaf(l0, al0, p00 + p10);
+      l1 = fmaf(l1, al1, p01 + p11);
+      // tokens past the length: p = 0, and their (unwritten) scales must not reach P'
+      const float va_s = va ? __half2float(vsp[gr]) : 0.f, vb_s = vb ? __half2float(vsp[gr + 8]) : 0.f;
+      const uint32_t pa = pack_half2(p00 * va_s, p01 * va_s);  // token gr: heads 2t, 2t+1
+      const uint32_t pb = pack_half2(p10 * vb_s, p11 * vb_s);  // token gr + 8
+      {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pa));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pb));
+        const float za = (float)vzp[gr], zb = (float)vzp[gr + 8];
+        z0 = fmaf(z0, al0, fmaf(fa.x, za, fb.x * zb));
+        z1 = fmaf(z1, al1, fmaf(fa.y, za, fb.y * zb));
       }
-      mma_16816(o[j], pa, codes_to_half2<BITS>(w, 0), codes_to_half2<BITS>(w, 1));
+      // B fragments of P' [16 tokens x 8 heads]: lane (gr, t) gets head gr at
+      // tokens 2t, 2t+1 and 2t+8, 2t+9
+      const uint32_t pb0 = movmatrix_trans(pa), pb1 = movmatrix_trans(pb);
+      if (rescale) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          o[p][0] *= al0;
+          o[p][1] *= al1;
+          o[p][2] *= al0;
+          o[p][3] *= al1;
+        }
+      }
+      // ---- out^T += V^T P'
+      constexpr int NC = BITS == 8 ? 4 : 2;
+      uint32_t vw[4 * NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(sp + SL::kV + warp * SL::kTile + c * 512 + lane * 16);
+        vw[4 * c] = u.x, vw[4 * c + 1] = u.y, vw[4 * c + 2] = u.z, vw[4 * c + 3] = u.w;
+      }
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        uint32_t a[4];
+        if constexpr (BITS == 8) {
+          a[0] = codes_to_half2<8>(vw[2 * p], 0);
+          a[1] = codes_to_half2<8>(vw[2 * p + 1], 0);
+          a[2] = codes_to_half2<8>(vw[2 * p], 1);
+          a[3] = codes_to_half2<8>(vw[2 * p + 1], 1);
+        } else {
+          a[0] = codes_to_half2<4>(vw[p], 0);
+          a[1] = codes_to_half2<4>(vw[p], 2);
+          a[2] = codes_to_half2<4>(vw[p], 1);
+          a[3] = codes_to_half2<4>(vw[p], 3);
+        }
+        mma_16816(o[p], a, pb0, pb1);
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * slot);  // the slot may be refilled
   }
-  // lane (gr, t): head gr, dimensions 8 j + 2 t, 8 j + 2 t + 1
-  lp += __shfl_xor_sync(0xffffffffu, lp, 1);
-  lp += __shfl_xor_sync(0xffffffffu, lp, 2);
-  zc += __shfl_xor_sync(0xffffffffu, zc, 1);
-  zc += __shfl_xor_sync(0xffffffffu, zc, 2);
-  if (head) {
-    if (t == 0) {
-      part[warp][gr][0] = m;
-      part[warp][gr][1] = lp;
-    }
+  // partial sums over this lane's tokens -> per head (over gr)
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      part[warp][gr][2 + 8 * j + 2 * t] = o[j][0] - zc;
-      part[warp][gr][2 + 8 * j + 2 * t + 1] = o[j][1] - zc;
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    z0 += __shfl_xor_sync(0xffffffffu, z0, x);
+    z1 += __shfl_xor_sync(0xffffffffu, z1, x);
+  }
+  __syncthreads();  // every slot consumed and landed: `part` may overlay the ring
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int h = 2 * t + hh;
+    if (h < G) {
+      float* pw = part + (warp * G + h) * kState;
+      if (gr == 0) {
+        pw[0] = hh ? m1 : m0;
+        pw[1] = hh ? l1 : l0;
+      }
+      const float zc = hh ? z1 : z0;
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        pw[2 + 16 * p + gr] = o[p][hh] - zc;
+        pw[2 + 16 * p + 8 + gr] = o[p][2 + hh] - zc;
+      }
     }
   }
   finish_attention<G>(part, cta, P, b, kvh, S, rank);
 }
 
-// Value codes token-major [B][L][Hkv][D bytes] -> dimension-major tiles
-// [B][Hkv][L/16][D][16 tokens] (int8) or [..][D][8 bytes] (int4, tokens
-// 2k and 2k+1 in the low and high nibble of byte k).
+// Value codes [B][Hkv][L][D * BITS / 8] -> tiles [B][Hkv][L / 16][16 * D *
+// BITS / 8] in the kernel's A-fragment order: 16-byte chunk (c, lane = 4 gr +
+// t) holds, for q of chunk c, the codes of dimension 8q + gr for tokens 2t,
+// 2t+1, 2t+8, 2t+9 -- int8: 4 chunks of 4 q, one byte per token; int4: 2
+// chunks of 8 q, 16 bits per q (tokens 2t, 2t+1 in the low and high nibble of
+// the first byte, 2t+8, 2t+9 in the second).
 template <int BITS>
 __global__ void kv_pack_v_kernel(const uint8_t* __restrict__ codes, int B, int L, int Hkv,
                                  uint8_t* __restrict__ tiles) {
   constexpr int RB = kAttnD * BITS / 8;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // (b, kvh, tile, dim)
-  const long long total = (long long)B * Hkv * (L / 16) * kAttnD;
+  constexpr int NC = BITS == 8 ? 4 : 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // ((bh, tile), c, lane)
+  const long long total = (long long)B * Hkv * (L / 16) * NC * 32;
   if (idx >= total) return;
-  const int dim = (int)(idx % kAttnD);
-  long long rest = idx / kAttnD;
-  const int tile = (int)(rest % (L / 16));
-  rest /= (L / 16);
-  const int kvh = (int)(rest % Hkv);
-  const int b = (int)(rest / Hkv);
-  uint32_t c[16];
+  const int lane = (int)(idx & 31), c = (int)((idx >> 5) % NC);
+  const long long tile = (idx >> 5) / NC;  // bh * L / 16 + tile in the sequence
+  const int gr = lane >> 2, t = lane & 3;
+  const uint8_t* src = codes + tile * 16 * RB;  // the tile's 16 token rows
+  auto code = [&](int tok, int dim) -> uint32_t {
+    if constexpr (BITS == 8) {
+      return src[tok * RB + dim];
+    } else {
+      return (src[tok * RB + dim / 2] >> (4 * (dim & 1))) & 15u;
+    }
+  };
+  uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint8_t byte = codes[(((size_t)b * L + tile * 16 + i) * Hkv + kvh) * RB + (BITS == 8 ? dim : dim / 2)];
-    c[i] = BITS == 8 ? byte : ((dim & 1) ? (byte >> 4) : (byte & 15u));
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (BITS == 8) {
+      const int dim = 8 * (4 * c + k) + gr;
+      w[k] = code(2 * t, dim) | (code(2 * t + 1, dim) << 8) | (code(2 * t + 8, dim) << 16) |
+             (code(2 * t + 9, dim) << 24);
+    } else {
+      w[k] = 0;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int dim = 8 * (8 * c + 2 * k + hb) + gr;
+        const uint32_t half = code(2 * t, dim) | (code(2 * t + 1, dim) << 4) | (code(2 * t + 8, dim) << 8) |
+                              (code(2 * t + 9, dim) << 12);
+        w[k] |= half << (16 * hb);
+      }
+    }
   }
-  if constexpr (BITS == 8) {
-    uint4 v;
-    v.x = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-    v.y = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-    v.z = c[8] | (c[9] << 8) | (c[10] << 16) | (c[11] << 24);
-    v.w = c[12] | (c[13] << 8) | (c[14] << 16) | (c[15] << 24);
-    reinterpret_cast<uint4*>(tiles)[idx] = v;
-  } else {
-    uint2 v;
-    v.x = c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12) | (c[4] << 16) | (c[5] << 20) | (c[6] << 24) | (c[7] << 28);
-    v.y = c[8] | (c[9] << 4) | (c[10] << 8) | (c[11] << 12) | (c[12] << 16) | (c[13] << 20) | (c[14] << 24) |
-          (c[15] << 28);
-    reinterpret_cast<uint2*>(tiles)[idx] = v;
-  }
+  reinterpret_cast<uint4*>(tiles)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 template <int BITS, int G>
 tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
+  constexpr uint32_t smem = KvSlot<BITS>::kSmem;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kv_attn_tc_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return TM_ERR_CUDA;
+    attr_set = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * P.Hkv), (unsigned)S, 1);
   cfg.blockDim = dim3(kAttnThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -386,7 +588,27 @@ tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, kv_attn_tc_kernel<BITS, G>, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
 }
 
+// CTAs resident on one SM for the attention kernel (shared memory bound).
+int attn_resident(uint32_t smem) {
+  int per_sm = 0, reserved = 0;
+  sm_shared_memory(0, &per_sm, &reserved);
+  const int r = per_sm / (int)(smem + reserved);
+  return r < 1 ? 1 : (r > 2 ? 2 : r);
+}
+
 }  // namespace
+
+cudaError_t kv_error_bits(uint32_t* bits, bool clear) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, s_err_kv, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (clear && v) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(s_err_kv, &zero, sizeof(zero));
+  }
+  *bits = v;
+  return e;
+}
 
 }  // namespace w4
 
@@ -427,18 +649,21 @@ extern "C" tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc
     return TM_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return TM_ERR_UNSUPPORTED;
-  if (split < 0 || split > max_split(G) || (split & (split - 1))) return TM_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(out)) & 3u) return TM_ERR_ALIGNMENT;
-  if ((reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & (bits == 8 ? 15u : 7u) ||
-      (reinterpret_cast<uintptr_t>(Q) & 7u))
-    return TM_ERR_ALIGNMENT;
+  if (split < 0 || split > kMaxSplit || (split & (split - 1))) return TM_ERR_INVALID_ARG;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(kc) |
+                        reinterpret_cast<uintptr_t>(ks) | reinterpret_cast<uintptr_t>(kz) |
+                        reinterpret_cast<uintptr_t>(vc) | reinterpret_cast<uintptr_t>(vs) |
+                        reinterpret_cast<uintptr_t>(vz);
+  if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(out) & 1u)) return TM_ERR_ALIGNMENT;
   if (B == 0) return TM_OK;
   int S = split;
   if (!S) {
-    // enough CTAs to cover the SMs twice, each with at least 256 tokens
-    const int sms = num_sms(0);
+    // split the tokens while the grid still fits in one wave of resident CTAs
+    // and every CTA keeps at least four slots of tokens
+    const uint32_t smem = bits == 8 ? KvSlot<8>::kSmem : KvSlot<4>::kSmem;
+    const long long slots = (long long)num_sms(0) * attn_resident(smem);
     S = 1;
-    while (S < max_split(G) && B * Hkv * S < 2 * sms && L / (2 * S) >= 256) S *= 2;
+    while (S < kMaxSplit && (long long)B * Hkv * S * 2 <= slots && L / (2 * S) >= 4 * 16 * kSlotTiles) S *= 2;
   }
   AttnParams P;
   P.Q = reinterpret_cast<const __half*>(Q);
@@ -474,8 +699,8 @@ extern "C" tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, i
                                   void* stream) {
   if (!codes || !tiles || B < 0 || L < 0 || Hkv <= 0 || L % 16 != 0 || (bits != 4 && bits != 8))
     return TM_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(tiles) & (bits == 8 ? 15u : 7u)) return TM_ERR_ALIGNMENT;
-  const long long total = (long long)B * Hkv * (L / 16) * kAttnD;
+  if (reinterpret_cast<uintptr_t>(tiles) & 15u) return TM_ERR_ALIGNMENT;
+  const long long total = (long long)B * Hkv * (L / 16) * (bits == 8 ? 4 : 2) * 32;
   if (total == 0) return TM_OK;
   const unsigned grid = (unsigned)((total + 255) / 256);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
