@@ -176,7 +176,7 @@ __device__ __forceinline__ void finish_attention(const float* part, float* cta, 
 #pragma unroll
       for (int w = 0; w < kConsumers; ++w) {
         const float m = part[(w * G + h) * kState];
-        const float s = m == -CUDART_INF_F ? 0.f : expf(m - mx);
+        const float s = m == -CUDART_INF_F ? 0.f : exp2f(m - mx);
         v = fmaf(part[(w * G + h) * kState + k], s, v);
       }
     }
@@ -202,7 +202,7 @@ __device__ __forceinline__ void finish_attention(const float* part, float* cta, 
       for (int r = 0; r < S; ++r) {
         const float m = cta[(r * G + h) * kState];
         if (m == -CUDART_INF_F) continue;
-        const float w = expf(m - mx);
+        const float w = exp2f(m - mx);
         den = fmaf(cta[(r * G + h) * kState + 1], w, den);
         num = fmaf(cta[(r * G + h) * kState + 2 + d], w, num);
       }
@@ -216,13 +216,18 @@ __device__ __forceinline__ void finish_attention(const float* part, float* cta, 
 // Per consumer warp one 16-token tile of each slot, on mma.m16n8k16 with the
 // tokens and the dimensions as the 16-row side and the (up to 8) query heads
 // of the KV head as the 8 columns, so no accumulator is wasted:
-//   scores^T [16 tokens x 8 heads] = K codes [16 x 128] . Q^T, 8 MMAs: the
-//     codes become exact fp16 integers (the fp16 pattern of 1024 OR-ed with a
-//     code, minus 1024) and score = s_k (Q . c - z_k sum Q) / sqrt(D) per
-//     token afterwards, in fp32.  The k order is permuted the same way on K
-//     and Q: in slice sl the slots 2t, 2t+1, 2t+8, 2t+9 of lane t hold
-//     dimensions 32t + 4sl .. 32t + 4sl + 3, so a lane reads the 32 dimensions
-//     it needs of a token with two (int8) or one (int4) 16-byte loads.
+//   scores^T [16 tokens x 8 heads] = K codes [16 x 128] . Q^T, 8 MMAs on the
+//     codes in their raw fp16 form: the pattern of 1024 OR-ed with an int8
+//     code is 1024 + c, an int4 code OR-ed in above the lowest nibble gives
+//     1024 + 16 c (its query entry is then taken / 16, exact), so the MMA sums
+//     Q . c plus a per-head constant (1024 times the query sum over the
+//     dimensions without the factor 16, 64 times the rest), removed with the
+//     zero point afterwards: score = s_k (Q . c - z_k sum Q) / sqrt(D), in
+//     fp32, kept in units of log2 (the softmax uses powers of two).  The k
+//     order is permuted the same way on K and Q: in slice sl the slots 2t,
+//     2t+1, 2t+8, 2t+9 of lane t hold dimensions 32t + 4sl .. 32t + 4sl + 3, so
+//     a lane reads the 32 dimensions it needs of a token with two (int8) or
+//     one (int4) 16-byte loads.
 //   out^T [128 dims x 8 heads] += V codes^T . P', 8 MMAs: P' = p s_v (rounded
 //     once to fp16) is the score fragment transposed by two movmatrix; the
 //     value tile holds, per lane, the codes of dimensions 8q + gr (q = 0..15)
@@ -242,6 +247,17 @@ __device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, int i) {
     const uint32_t x = __byte_perm(w, 0u, 0x4040u | (uint32_t)i | ((uint32_t)i << 8));  // byte i in bytes 0 and 2
     const uint32_t y = lop3<0xEA>(x, 0x00F0000Fu, 0x64006400u);  // (1024 + lo, 1024 + 16 hi)
     return hfma2_u32(y, 0x2C003C00u, 0xD400E400u);              // (x - 1024, x / 16 - 64)
+  }
+}
+
+// Raw form of the key codes for the score MMA: int8 bytes 2i, 2i+1 of w ->
+// (1024 + c0, 1024 + c1); int4 byte i -> (1024 + lo, 1024 + 16 hi).
+template <int BITS>
+__device__ __forceinline__ uint32_t codes_raw(uint32_t w, int i) {
+  if constexpr (BITS == 8) {
+    return __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);
+  } else {
+    return lop3<0xEA>(__byte_perm(w, 0u, 0x4040u | (uint32_t)i | ((uint32_t)i << 8)), 0x00F0000Fu, 0x64006400u);
   }
 }
 
@@ -323,10 +339,11 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
 
   // ---- consumers
   const int gr = lane >> 2, t = lane & 3;
-  // B fragments of Q^T (column gr = query head gr < G) in the permuted k order,
-  // and sum_d Q[h][d] for this lane's heads 2t, 2t+1
+  // B fragments of Q^T (column gr = query head gr < G) in the permuted k order
+  // (int4: odd dimensions / 16); for this lane's heads 2t, 2t+1 the sum of Q
+  // over the dimensions and the constant the raw codes add to the MMA sum
   uint32_t qb[8][2];
-  float qs0, qs1;
+  float qs0, qs1, off0, off1;
   {
     uint4 q4[4] = {};
     if (gr < G) {
@@ -334,26 +351,35 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) q4[c] = qp[c];
     }
-    float qsum = 0.f;
+    float qe = 0.f, qo = 0.f;  // sums over even and odd dimensions
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint32_t wv[4] = {q4[c].x, q4[c].y, q4[c].z, q4[c].w};
+      uint32_t wv[4] = {q4[c].x, q4[c].y, q4[c].z, q4[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-        qsum += f.x + f.y;
+        qe += f.x;
+        qo += f.y;
+        if constexpr (BITS == 4) wv[e] = hmul2_u32(wv[e], 0x2C003C00u);  // (x, y / 16), exact
       }
       qb[2 * c][0] = wv[0];
       qb[2 * c][1] = wv[1];
       qb[2 * c + 1][0] = wv[2];
       qb[2 * c + 1][1] = wv[3];
     }
-    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);  // head gr
-    qs0 = __shfl_sync(0xffffffffu, qsum, 8 * t);      // head 2t
+#pragma unroll
+    for (int x = 1; x <= 2; x <<= 1) {
+      qe += __shfl_xor_sync(0xffffffffu, qe, x);
+      qo += __shfl_xor_sync(0xffffffffu, qo, x);
+    }
+    const float qsum = qe + qo;                                  // head gr
+    const float off = 1024.f * qe + (BITS == 8 ? 1024.f : 64.f) * qo;
+    qs0 = __shfl_sync(0xffffffffu, qsum, 8 * t);  // head 2t
     qs1 = __shfl_sync(0xffffffffu, qsum, 8 * t + 4);  // head 2t + 1
+    off0 = __shfl_sync(0xffffffffu, off, 8 * t);
+    off1 = __shfl_sync(0xffffffffu, off, 8 * t + 4);
   }
-  const float scale = rsqrtf((float)kAttnD);
+  const float scale = rsqrtf((float)kAttnD) * 1.4426950408889634f;  // 1 / sqrt(D), in log2 units
 
   // heads 2t, 2t+1: running max, and this lane's partial sums of p and p' z
   float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
@@ -375,13 +401,10 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
         const uint8_t* ka = sp + SL::kK + (warp * 16 + gr) * RB;
         const uint8_t* kb = ka + 8 * RB;
         if constexpr (BITS == 8) {
-          // odd rows read their two halves in the other order: no bank conflict
-          const int h = gr & 1;
-          const uint4 a0 = *reinterpret_cast<const uint4*>(ka + 32 * t + 16 * h);
-          const uint4 a1 = *reinterpret_cast<const uint4*>(ka + 32 * t + 16 * (h ^ 1));
-          const uint4 b0 = *reinterpret_cast<const uint4*>(kb + 32 * t + 16 * h);
-          const uint4 b1 = *reinterpret_cast<const uint4*>(kb + 32 * t + 16 * (h ^ 1));
-          const uint4 alo = h ? a1 : a0, ahi = h ? a0 : a1, blo = h ? b1 : b0, bhi = h ? b0 : b1;
+          const uint4 alo = *reinterpret_cast<const uint4*>(ka + 32 * t);
+          const uint4 ahi = *reinterpret_cast<const uint4*>(ka + 32 * t + 16);
+          const uint4 blo = *reinterpret_cast<const uint4*>(kb + 32 * t);
+          const uint4 bhi = *reinterpret_cast<const uint4*>(kb + 32 * t + 16);
           wa[0] = alo.x, wa[1] = alo.y, wa[2] = alo.z, wa[3] = alo.w;
           wa[4] = ahi.x, wa[5] = ahi.y, wa[6] = ahi.z, wa[7] = ahi.w;
           wb[0] = blo.x, wb[1] = blo.y, wb[2] = blo.z, wb[3] = blo.w;
@@ -398,16 +421,16 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       for (int sl = 0; sl < 8; ++sl) {
         uint32_t a[4];
         if constexpr (BITS == 8) {
-          a[0] = codes_to_half2<8>(wa[sl], 0);
-          a[1] = codes_to_half2<8>(wb[sl], 0);
-          a[2] = codes_to_half2<8>(wa[sl], 1);
-          a[3] = codes_to_half2<8>(wb[sl], 1);
+          a[0] = codes_raw<8>(wa[sl], 0);
+          a[1] = codes_raw<8>(wb[sl], 0);
+          a[2] = codes_raw<8>(wa[sl], 1);
+          a[3] = codes_raw<8>(wb[sl], 1);
         } else {
           const int by = 2 * (sl & 1);
-          a[0] = codes_to_half2<4>(wa[sl >> 1], by);
-          a[1] = codes_to_half2<4>(wb[sl >> 1], by);
-          a[2] = codes_to_half2<4>(wa[sl >> 1], by + 1);
-          a[3] = codes_to_half2<4>(wb[sl >> 1], by + 1);
+          a[0] = codes_raw<4>(wa[sl >> 1], by);
+          a[1] = codes_raw<4>(wb[sl >> 1], by);
+          a[2] = codes_raw<4>(wa[sl >> 1], by + 1);
+          a[3] = codes_raw<4>(wb[sl >> 1], by + 1);
         }
         mma_16816((sl & 1) ? d1 : d0, a, qb[sl][0], qb[sl][1]);
       }
@@ -419,10 +442,11 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       const bool va = t0 + gr < t_end, vb = t0 + gr + 8 < t_end;
       const float ka_s = __half2float(ksp[gr]) * scale, kb_s = __half2float(ksp[gr + 8]) * scale;
       const float ka_z = (float)kzp[gr], kb_z = (float)kzp[gr + 8];
-      const float s00 = va ? ka_s * fmaf(-ka_z, qs0, d0[0] + d1[0]) : -CUDART_INF_F;  // token gr, head 2t
-      const float s01 = va ? ka_s * fmaf(-ka_z, qs1, d0[1] + d1[1]) : -CUDART_INF_F;  // token gr, head 2t+1
-      const float s10 = vb ? kb_s * fmaf(-kb_z, qs0, d0[2] + d1[2]) : -CUDART_INF_F;  // token gr+8, head 2t
-      const float s11 = vb ? kb_s * fmaf(-kb_z, qs1, d0[3] + d1[3]) : -CUDART_INF_F;  // token gr+8, head 2t+1
+      // Q . c = raw sum - off; minus z_k sum Q
+      const float s00 = va ? ka_s * (fmaf(-ka_z, qs0, d0[0] + d1[0]) - off0) : -CUDART_INF_F;  // token gr, head 2t
+      const float s01 = va ? ka_s * (fmaf(-ka_z, qs1, d0[1] + d1[1]) - off1) : -CUDART_INF_F;  // token gr, head 2t+1
+      const float s10 = vb ? kb_s * (fmaf(-kb_z, qs0, d0[2] + d1[2]) - off0) : -CUDART_INF_F;  // token gr+8, head 2t
+      const float s11 = vb ? kb_s * (fmaf(-kb_z, qs1, d0[3] + d1[3]) - off1) : -CUDART_INF_F;  // token gr+8, head 2t+1
       float mt0 = fmaxf(s00, s10), mt1 = fmaxf(s01, s11);
 #pragma unroll
       for (int x = 4; x < 32; x <<= 1) {
@@ -431,10 +455,10 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       }
       const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);  // finite: token t0 is valid
       const bool rescale = !__all_sync(0xffffffffu, mn0 == m0 && mn1 == m1);
-      const float al0 = expf(m0 - mn0), al1 = expf(m1 - mn1);  // 0 on the first tile
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);  // 0 on the first tile
       m0 = mn0;
       m1 = mn1;
-      const float p00 = expf(s00 - mn0), p01 = expf(s01 - mn1), p10 = expf(s10 - mn0), p11 = expf(s11 - mn1);
+      const float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1), p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
       l0 = fmaf(l0, al0, p00 + p10);
       l1 = fmaf(l1, al1, p01 + p11);
       // tokens past the length: p = 0, and their (unwritten) scales must not reach P'
