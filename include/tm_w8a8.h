@@ -1,0 +1,84 @@
+/*
+ * W8A8 GEMM: 8-bit integer weights and activations ("LMDeploy Guide: Fast
+ * Mixed-Precision LLM Inference Engine": W8A8 among the precision formats
+ * the engine serves, from SmoothQuant-style post-training quantisation).
+ *
+ * The scheme (our reading; the smoothing factors are folded into the fp16
+ * weights beforehand): activations quantised per token, dynamically; weights
+ * per output channel; both symmetric, in IEEE binary32 with
+ * round-to-nearest-even at each step:
+ *   a = max |x| over the row (column);  s = a / 127, or 1 when a == 0
+ *   i = 1 / s;  q = clamp(rint(x * i), -127, 127)
+ *   Y[m][n] = fp16( s_x[m] * s_w[n] * sum_k q_x[m][k] q_w[k][n] )
+ * The integer products are exact on the tensor cores (fp16 operands holding
+ * the integers, fp32 accumulation: exact while a partial sum stays below
+ * 2^24); the scaling is one fp32 product per output.
+ *
+ * Conventions as in tm_w4a16.h: device pointers, asynchronous on `stream`
+ * (a cudaStream_t, NULL = legacy default stream) unless stated otherwise,
+ * no allocation outside tm_w8_pack.
+ */
+#ifndef TM_W8A8_H
+#define TM_W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tm_w4a16.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque packed 8-bit weights (codes in the kernel's fragment order and the
+ * per-channel scales), one device allocation. */
+typedef struct tm_w8_packed tm_w8_packed;
+
+/*
+ * Per-token dynamic quantisation of the activations (the rule above, per row).
+ *   X : device fp16 bits [M][K] row-major, 16-byte aligned; K % 16 == 0
+ *   xq: device int8 [M][K], 16-byte aligned;  sx: device fp32 [M], 4-byte aligned
+ * One launch; TM_ERR_INVALID_ARG on a bad shape, TM_ERR_ALIGNMENT on a
+ * misaligned pointer.
+ */
+tm_status tm_w8a8_quantize_act(const uint16_t* X, int M, int K, int8_t* xq, float* sx, void* stream);
+
+/*
+ * Offline repack of per-channel quantised weights into the GEMM's order.
+ *   q : device int8 [K][N] row-major (codes -127..127)
+ *   sw: device fp32 [N]
+ *   K % 16 == 0, N % 16 == 0; K is padded to a multiple of 128 with zero codes.
+ * Synchronous on the current device; the caller frees the handle with
+ * tm_w8_packed_free.
+ */
+tm_status tm_w8_pack(const int8_t* q, const float* sw, int K, int N, tm_w8_packed** out);
+
+/* Inverse of tm_w8_pack into device buffers with its input layouts
+ * (synchronous; pack -> unpack is bit-exact). */
+tm_status tm_w8_unpack(const tm_w8_packed* p, int8_t* q, float* sw);
+
+/* K, N and the bytes of the device allocation of a handle (any out pointer may be NULL). */
+tm_status tm_w8_packed_info(const tm_w8_packed* p, int* K, int* N, size_t* bytes);
+
+/* Release a handle (NULL is ignored). */
+void tm_w8_packed_free(tm_w8_packed* p);
+
+/*
+ * Y = fp16(s_x s_w^T . (q_x q_w)), one launch.
+ *   xq: device int8 [M][K] (from tm_w8a8_quantize_act), 16-byte aligned
+ *   sx: device fp32 [M];  Y: device fp16 [M][N] row-major, 16-byte aligned
+ *   split_k: 0 automatic, else 1, 2, 4 or 8 CTAs (a thread-block cluster)
+ *            sharing one output tile along K, reduced through distributed
+ *            shared memory (no global workspace)
+ * M up to 32 rows run in one row tile (decode), larger M in tiles of 64 rows.
+ * Waits are bounded: a copy that never lands sets the device timeout bit
+ * (tm_device_error).
+ */
+tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
+                       void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TM_W8A8_H */

@@ -1,4 +1,5 @@
-"""Thin ctypes binding of ``include/tm_w4a16.h`` (argument marshalling only).
+"""Thin ctypes binding of ``include/tm_w4a16.h`` and ``include/tm_w8a8.h``
+(argument marshalling only).
 
 Every step of the computation runs in the CUDA library; PyTorch provides
 device memory and streams.  If the library is missing this module raises --
@@ -21,7 +22,8 @@ _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
-           "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v")
+           "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
+           "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm")
 
 
 class TMError(RuntimeError):
@@ -91,6 +93,18 @@ def load(path: Optional[str] = None):
     lib.tm_w4a16_gemm_silu_mul.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
     lib.tm_quantize_rtn.restype = ci
     lib.tm_quantize_rtn.argtypes = [vp, ci, ci, ci, vp, vp, vp, vp]
+    lib.tm_w8a8_quantize_act.restype = ci
+    lib.tm_w8a8_quantize_act.argtypes = [vp, ci, ci, vp, vp, vp]
+    lib.tm_w8_pack.restype = ci
+    lib.tm_w8_pack.argtypes = [vp, vp, ci, ci, ctypes.POINTER(vp)]
+    lib.tm_w8_unpack.restype = ci
+    lib.tm_w8_unpack.argtypes = [vp, vp, vp]
+    lib.tm_w8_packed_info.restype = ci
+    lib.tm_w8_packed_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(csz)]
+    lib.tm_w8_packed_free.restype = None
+    lib.tm_w8_packed_free.argtypes = [vp]
+    lib.tm_w8a8_gemm.restype = ci
+    lib.tm_w8a8_gemm.argtypes = [vp, vp, vp, vp, ci, ci, vp]
     _lib = lib
     return lib
 
@@ -338,3 +352,82 @@ def device_error(clear: bool = True) -> int:
 
 def last_launch_count() -> int:
     return load().tm_last_launch_count()
+
+
+# ------------------------------------------------------------------ W8A8 ---
+
+def w8a8_quantize_act(X: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """Per-token int8 quantisation of fp16 X [M][K] (see tm_w8a8_quantize_act):
+    returns (xq int8 [M][K], sx fp32 [M])."""
+    if X.dim() != 2 or X.dtype != torch.float16:
+        raise ValueError("X must be fp16 [M][K]")
+    M, K = X.shape
+    xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    st = stream if stream is not None else torch.cuda.current_stream(X.device)
+    _check(load().tm_w8a8_quantize_act(_dev(X, torch.float16, "X"), M, K, xq.data_ptr(), sx.data_ptr(),
+                                       ctypes.c_void_p(st.cuda_stream)), "tm_w8a8_quantize_act")
+    return xq, sx
+
+
+class W8Packed:
+    """Owns a ``tm_w8_packed`` handle (device memory on the device of ``q``)."""
+
+    def __init__(self, q: torch.Tensor, sw: torch.Tensor):
+        lib = load()
+        K, N = q.shape
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(q.device):
+            st = lib.tm_w8_pack(_dev(q, torch.int8, "q"), _dev(sw, torch.float32, "sw"), K, N, ctypes.byref(handle))
+        _check(st, "tm_w8_pack")
+        self._h = handle
+        self.K, self.N = K, N
+        self.device = q.device
+        b = ctypes.c_size_t()
+        _check(lib.tm_w8_packed_info(handle, None, None, ctypes.byref(b)), "tm_w8_packed_info")
+        self.nbytes = b.value
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("packed weights were freed")
+        return self._h
+
+    def unpack(self):
+        q = torch.empty((self.K, self.N), dtype=torch.int8, device=self.device)
+        sw = torch.empty((self.N,), dtype=torch.float32, device=self.device)
+        with torch.cuda.device(self.device):
+            _check(load().tm_w8_unpack(self.handle, q.data_ptr(), sw.data_ptr()), "tm_w8_unpack")
+        return q, sw
+
+    def free(self):
+        if self._h is not None:
+            load().tm_w8_packed_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def pack_w8(q: torch.Tensor, sw: torch.Tensor) -> W8Packed:
+    return W8Packed(q, sw)
+
+
+def w8a8_gemm(xq: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[torch.Tensor] = None, split: int = 0,
+              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Y = fp16(sx sw^T (xq . q_w)) for int8 xq [M][K] and fp32 sx [M] (tm_w8a8_gemm)."""
+    if xq.dim() != 2 or xq.shape[1] != w.K:
+        raise ValueError("xq must be int8 [M][K]")
+    M = xq.shape[0]
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float16, device=xq.device)
+    if tuple(out.shape) != (M, w.N):
+        raise ValueError("out must be fp16 [M][N]")
+    st = stream if stream is not None else torch.cuda.current_stream(xq.device)
+    _check(load().tm_w8a8_gemm(_dev(xq, torch.int8, "xq"), _dev(sx, torch.float32, "sx"), w.handle,
+                               _dev(out, torch.float16, "out"), M, split, ctypes.c_void_p(st.cuda_stream)),
+           "tm_w8a8_gemm")
+    return out
