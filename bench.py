@@ -828,6 +828,128 @@ def run_kv(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+def run_w8a8(args, rank, world, local, prefill=False):
+    """--workload w8a8 / w8a8_prefill: the W8A8 path on the four Llama-3-8B
+    linear shapes -- per GEMM, the per-token activation quantiser
+    (tm_w8a8_quantize_act) then the GEMM (tm_w8a8_gemm) -- at the decode sizes
+    M in {1, 8, 16, 32} (GB/s of algorithmic bytes against the measured HBM
+    bandwidth) or the prefill sizes M in {128, 1024, 4096} (TFLOP/s against
+    the measured bf16 peak: the products run on fp16 tensor cores).  One step =
+    every (shape, M) pair, each with its own packed weights, graph-replayed."""
+    import numpy as np
+    import torch
+
+    import oracle.w8a8 as w8_oracle
+    from w4a16_quantized_gemm_gb300 import binding, synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    binding.load()
+    peaks = load_peaks()
+    Ms = (128, 1024, 4096) if prefill else (1, 8, 16, 32)
+    host = {}
+    items = []
+    for name in ("qkv", "o_proj", "gate_up", "down"):
+        K, N = synth.LLAMA3_8B[name]
+        W = (synth.normal64(f"w8bench/W/{name}", K, N) * 0.02).astype(np.float16)
+        q, sw = w8_oracle.quantize_weight(W)
+        del W
+        host[name] = (q, sw)
+        qd, sd = torch.from_numpy(q).to(device), torch.from_numpy(sw).to(device)
+        for M in Ms:
+            X = torch.from_numpy(synth.activations(M, K, tag=f"/w8/{name}/M{M}").view(np.uint16)).to(device)
+            X = X.view(torch.float16)
+            items.append({"name": name, "M": M, "K": K, "N": N, "w": binding.pack_w8(qd, sd), "X": X,
+                          "xq": torch.empty((M, K), dtype=torch.int8, device=device),
+                          "sx": torch.empty((M,), dtype=torch.float32, device=device),
+                          "Y": torch.empty((M, N), dtype=torch.float16, device=device),
+                          "bytes": 2 * M * K + M * K + 4 * M + w8_oracle.algorithmic_bytes(M, K, N),
+                          "flops": 2 * M * K * N})
+        del qd, sd
+    step_bytes = sum(it["bytes"] for it in items)
+    step_flops = sum(it["flops"] for it in items)
+    weight_bytes = sum(it["w"].nbytes for it in items)
+    stream = torch.cuda.Stream(device)
+
+    def launch_all(st):
+        for it in items:
+            binding.w8a8_quantize_act(it["X"], out=(it["xq"], it["sx"]), stream=st)
+            binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
+
+    with torch.cuda.stream(stream):
+        launch_all(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        launch_all(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t_ms = e0.elapsed_time(e1)
+    with torch.cuda.stream(stream):
+        while time.time() - t0 < 1.5:
+            for _ in range(20):
+                graph.replay()
+            stream.synchronize()
+    clocks = sampler.stop()
+    t_max_s = reduce_max(t_ms / 1e3, world)
+    step_s = t_ms / 1e3 / args.steps
+    if prefill:
+        value = aggregate(step_flops * args.steps / 1e12, world, t_max_s)
+        achieved = step_flops / step_s / 1e12
+        peak, unit, bound = peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+    else:
+        value = aggregate(step_bytes * args.steps / 1e9, world, t_max_s)
+        achieved = step_bytes / step_s / 1e9
+        peak, unit, bound = peaks["hbm_gbs"], "GB/s", "hbm"
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        # the oracle (binary32 quantiser, exact int64 product) on the first
+        # `cols` output columns of every GEMM of the step, scaled by N / cols
+        cols = 64 if prefill else 2048
+        t_sample = t_full = 0.0
+        for it in items:
+            q, sw = host[it["name"]]
+            Xh = it["X"].cpu().numpy()
+            ts = time.perf_counter()
+            qx, sx = w8_oracle.quantize_act(Xh)
+            w8_oracle.gemm(qx, sx, q[:, :cols], sw[:cols])
+            dt = time.perf_counter() - ts
+            t_sample += dt
+            t_full += dt * it["N"] / cols
+        units = step_flops / 1e12 if prefill else step_bytes / 1e9
+        cpu = {"value": round(units / t_full, 6), "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": f"every GEMM of one step on its first {cols} output columns (all rows, full K), "
+                         f"{t_sample:.1f} s measured, scaled by N/{cols} per GEMM to a full step ({t_full:.1f} s)"}
+    label = "prefill, M in {128,1024,4096}" if prefill else "decode, M in {1,8,16,32}"
+    out = {
+        "metric": f"W8A8 {unit}, Llama-3-8B linear layers, {label} (per-token quantiser + GEMM)",
+        "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"w8a8{'_prefill' if prefill else ''}: qkv, o_proj, gate_up, down x M",
+                   "launches_per_step": 2 * len(items), "bytes_per_step": step_bytes, "flops_per_step": step_flops,
+                   "l2": f"each GEMM has its own packed weights ({weight_bytes / 1e6:.0f} MB per step > 129 MB L2)"},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peaks["source"],
+                     "kernel": "w8_kernel (+ w8_quant_act_kernel), whole step"},
+        "gpu_launches": 2 * len(items) * args.steps, "clocks": clocks, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_rtn_reference(args, rank):
     """Reference arm of --workload rtn: the binary32 oracle on the host."""
     if rank != 0:
@@ -891,7 +1013,8 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu", "kv"], default="decode")
+    p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu", "kv", "w8a8", "w8a8_prefill"],
+                   default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
@@ -910,10 +1033,10 @@ def main(argv=None):
     if args.impl == "reference":
         if args.workload == "rtn":
             run_rtn_reference(args, rank)
-        elif args.workload in ("silu", "kv"):
+        elif args.workload in ("silu", "kv", "w8a8", "w8a8_prefill"):
             if rank == 0:
-                print(json.dumps({"impl": "reference", "unavailable": "the silu workload's reference arm is the "
-                                  "oracle timed by the default decode workload"}), flush=True)
+                print(json.dumps({"impl": "reference", "unavailable": f"the {args.workload} workload reports its "
+                                  "oracle timing as cpu_baseline on its own line"}), flush=True)
         else:
             run_reference(args, rank, world)
         return
@@ -929,6 +1052,8 @@ def main(argv=None):
             run_silu(args, rank, world, local)
         elif args.workload == "kv":
             run_kv(args, rank, world, local)
+        elif args.workload in ("w8a8", "w8a8_prefill"):
+            run_w8a8(args, rank, world, local, prefill=args.workload == "w8a8_prefill")
         else:
             run_gpu(args, rank, world, local)
     finally:

@@ -356,17 +356,23 @@ def last_launch_count() -> int:
 
 # ------------------------------------------------------------------ W8A8 ---
 
-def w8a8_quantize_act(X: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+def w8a8_quantize_act(X: torch.Tensor, out: Optional[tuple] = None, stream: Optional[torch.cuda.Stream] = None):
     """Per-token int8 quantisation of fp16 X [M][K] (see tm_w8a8_quantize_act):
-    returns (xq int8 [M][K], sx fp32 [M])."""
+    returns (xq int8 [M][K], sx fp32 [M]), into `out` when given."""
     if X.dim() != 2 or X.dtype != torch.float16:
         raise ValueError("X must be fp16 [M][K]")
     M, K = X.shape
-    xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
-    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    if out is None:
+        xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    else:
+        xq, sx = out
+        if tuple(xq.shape) != (M, K) or tuple(sx.shape) != (M,):
+            raise ValueError("out must be (int8 [M][K], fp32 [M])")
     st = stream if stream is not None else torch.cuda.current_stream(X.device)
-    _check(load().tm_w8a8_quantize_act(_dev(X, torch.float16, "X"), M, K, xq.data_ptr(), sx.data_ptr(),
-                                       ctypes.c_void_p(st.cuda_stream)), "tm_w8a8_quantize_act")
+    _check(load().tm_w8a8_quantize_act(_dev(X, torch.float16, "X"), M, K, _dev(xq, torch.int8, "xq"),
+                                       _dev(sx, torch.float32, "sx"), ctypes.c_void_p(st.cuda_stream)),
+           "tm_w8a8_quantize_act")
     return xq, sx
 
 
