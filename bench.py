@@ -43,7 +43,8 @@ WORKLOADS = {
     "prefill": {"idx": 2, "unit": "TFLOP/s", "bound": "tensor",
                 "name": "llama3-8b prefill linears: qkv/o_proj/gate_up/down x M in {128,1024,4096}, g=128"},
 }
-KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "tc": ["tc.cu", "tm_common.cuh"]}
+KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "tc": ["tc.cu", "tm_common.cuh"],
+                  "kv": ["kv.cu", "tm_common.cuh"], "w8": ["w8a8.cu", "tm_common.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -820,7 +821,7 @@ def run_kv(args, rank, world, local):
                    "launches_per_step": 2, "bytes_per_step": step_bytes,
                    "l2": f"inputs larger than L2 ({step_bytes / 1e6:.0f} MB of cache per step)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": read_traffic("kv", "llama3_8b_kv"),
                      "peak_source": peaks["source"], "kernel": "kv_attn_tc_kernel"},
         "gpu_launches": 2 * args.steps, "clocks": clocks, "cpu_baseline": cpu,
     }

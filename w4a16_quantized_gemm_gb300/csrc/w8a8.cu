@@ -61,9 +61,14 @@ constexpr uint32_t kW8SmemMax = 227 * 1024;
 // ---------------------------------------------------------- quantisers -----
 
 // One CTA per row of X [M][K] (K % 8 == 0): the row's max |x|, then the codes.
+// Under programmatic dependent launch the next grid (the GEMM, which streams
+// its weights first) may start at once; X is read and xq, sx written only
+// after the preceding grid finished.
 __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restrict__ X, int K,
                                                             int8_t* __restrict__ q, float* __restrict__ sx) {
   __shared__ float red[8];
+  launch_dependents();
+  grid_dependency_wait();
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + (size_t)m * K);
   const int nv = K / 8;
@@ -437,9 +442,17 @@ extern "C" tm_status tm_w8a8_quantize_act(const uint16_t* X, int M, int K, int8_
       (reinterpret_cast<uintptr_t>(sx) & 3u))
     return TM_ERR_ALIGNMENT;
   if (M == 0) return TM_OK;
-  w8_quant_act_kernel<<<(unsigned)M, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      reinterpret_cast<const __half*>(X), K, xq, sx);
-  if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, w8_quant_act_kernel, reinterpret_cast<const __half*>(X), K, xq, sx) != cudaSuccess)
+    return TM_ERR_CUDA;
   set_launch_count(1);
   return TM_OK;
 }
