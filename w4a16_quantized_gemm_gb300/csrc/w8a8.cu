@@ -21,16 +21,17 @@
 // cluster reduce through distributed shared memory; the epilogue applies
 // s_x[m] s_w[n] and rounds to fp16 once.
 //
-// Packed weights (ours): K padded to Kp, a multiple of 128 (zero codes);
-// a unit is 16 columns (an n-tile) x 64 k = 1 KB, stored as two halves of
-// 32 lanes x 16 bytes.  Lane l = 4 gr + t, half h holds four words: word
-// 2 s2 + r (s2 = 0, 1) is step st = 2h + s2 for row gr + 8r, bytes j = 0..3
-// the codes of k = 16t + 4st + j (biased: q + 128).  One word pair is one
-// mma.m16n8k16 A fragment of W^T once the step's k order is permuted the same
-// way on X (slots 2t, 2t+1, 2t+8, 2t+9 -> k 16t + 4st + 0..3), so a lane's B
-// fragments for the four steps of a unit are the 16 bytes at 16t of each X
-// row.  Units are ordered [Kp/128][N/16][2]: the codes of one 128-k block for
-// consecutive n-tiles are one contiguous run.
+// Packed weights (ours): W^T in blocks of 128 k, [Kp/128][N][128 bytes] --
+// row n of a block holds the codes (biased: q + 128) of column n for those
+// 128 k, K padded to Kp, a multiple of 128, with zero codes.  The kernels load
+// 128 rows (8 n-tiles) of a block with one TMA box and the 128-byte swizzle
+// (16-byte chunk c of row r stored at c ^ (r & 7)), which makes both reads
+// conflict-free: the mma.sync path takes, for lane 4 gr + t, the 16 bytes at
+// k 16t of rows gr and gr + 8 -- word st of each is the step-st A fragment
+// once the step's k order is permuted the same way on X (slots 2t, 2t+1, 2t+8,
+// 2t+9 -> k 16t + 4st + 0..3), so a lane's B fragments for a 64-k unit are the
+// 16 bytes at 16t of an X row; the tensor-memory path has each thread convert
+// its own row.
 #include <algorithm>
 #include <new>
 
@@ -40,10 +41,11 @@
 struct tm_w8_packed {
   int K, N, Kp, NT, KB;
   int device;
-  uint8_t* codes;  // [KB][NT][2048]
+  uint8_t* codes;  // [KB][N][128]
   float* scales;   // [N]
   void* base;
   size_t bytes;
+  CUtensorMap tm_codes;  // u8 {128, N, KB}, box {128, 128, 1}, 128-byte swizzle
 };
 
 namespace w4 {
@@ -110,23 +112,21 @@ __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restr
 
 // ------------------------------------------------------------- packing -----
 
-// One thread per 16-byte chunk of the packed codes (see the layout above).
-__global__ void w8_pack_kernel(const int8_t* __restrict__ q, int K, int N, int NT, long long chunks,
-                               uint4* __restrict__ out) {
+// One thread per 16-byte chunk of the packed codes: chunk c of row n of block
+// kb holds the biased codes of column n at k = 128 kb + 16c .. +15.
+__global__ void w8_pack_kernel(const int8_t* __restrict__ q, int K, int N, long long chunks, uint4* __restrict__ out) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= chunks) return;
-  const int lane = (int)(idx & 31), h = (int)((idx >> 5) & 1), u = (int)((idx >> 6) & 1);
-  const long long blk = idx >> 7;  // kb * NT + nt
-  const int nt = (int)(blk % NT), kb = (int)(blk / NT);
-  const int gr = lane >> 2, t = lane & 3;
+  const int c = (int)(idx & 7);
+  const long long row = idx >> 3;  // kb * N + n
+  const int n = (int)(row % N), kb = (int)(row / N);
   uint32_t w[4];
 #pragma unroll
   for (int wi = 0; wi < 4; ++wi) {
-    const int st = 2 * h + (wi >> 1), n = nt * 16 + gr + 8 * (wi & 1);
     uint32_t v = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int k = kb * 128 + u * 64 + 16 * t + 4 * st + j;
+      const int k = kb * 128 + 16 * c + 4 * wi + j;
       const int code = k < K ? (int)q[(size_t)k * N + n] : 0;
       v |= (uint32_t)((code + 128) & 0xFF) << (8 * j);
     }
@@ -135,16 +135,11 @@ __global__ void w8_pack_kernel(const int8_t* __restrict__ q, int K, int N, int N
   out[idx] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__global__ void w8_unpack_kernel(const uint8_t* __restrict__ codes, int K, int N, int NT, int8_t* __restrict__ q) {
+__global__ void w8_unpack_kernel(const uint8_t* __restrict__ codes, int K, int N, int8_t* __restrict__ q) {
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)K * N) return;
   const int k = (int)(idx / N), n = (int)(idx % N);
-  const int kb = k / 128, u = (k / 64) & 1, kk = k & 63;
-  const int t = kk / 16, st = (kk / 4) & 3, j = kk & 3;
-  const int nt = n / 16, r = (n & 15) >= 8 ? 1 : 0, gr = n & 7;
-  const int h = st >> 1, wi = 2 * (st & 1) + r;
-  const size_t off = ((((size_t)kb * NT + nt) * 2 + u) * 2 + h) * 512 + (size_t)(4 * gr + t) * 16 + wi * 4 + j;
-  q[idx] = (int8_t)((int)codes[off] - 128);
+  q[idx] = (int8_t)((int)codes[((size_t)(k / 128) * N + n) * 128 + (k & 127)] - 128);
 }
 
 // --------------------------------------------------------------- GEMM ------
@@ -181,6 +176,7 @@ __device__ __forceinline__ bool w8_drain(uint32_t bar, uint32_t parity) {
 // MT: 8-row tiles of X per CTA (8 MT rows from row blockIdx.x * 8 MT).
 template <int MT>
 __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                              const __grid_constant__ CUtensorMap tmW,
                                                               const W8Params P) {
   constexpr int CNN = kW8CN * 16;
   extern __shared__ uint8_t smem_raw[];
@@ -216,12 +212,11 @@ __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_const
     // ---------------- producer: one elected thread ----------------
     if (lane == 0) {
       prefetch_tmap(&tmX);
-      const int nvalid = min(kW8CN, P.NT - nt0);
-      const uint32_t tx = P.x_bytes + (uint32_t)nvalid * kW8Block;
+      prefetch_tmap(&tmW);
+      const uint32_t tx = P.x_bytes + kW8CN * kW8Block;  // boxes count in full, zero-filled past N and K
       auto issue_w = [&](int i) {
-        const uint32_t st = base + (i % stages) * P.stage_bytes;
-        const size_t blk = (size_t)(kb_begin + i) * P.NT + nt0;
-        bulk_g2s(st + P.x_bytes, P.codes + blk * kW8Block, (uint32_t)nvalid * kW8Block, bar_full + 8 * (i % stages));
+        tma_load_3d(base + (i % stages) * P.stage_bytes + P.x_bytes, &tmW, 0, nt0 * 16, kb_begin + i,
+                    bar_full + 8 * (i % stages));
       };
       auto issue_x = [&](int i) {
         tma_load_2d(base + (i % stages) * P.stage_bytes, &tmX, (kb_begin + i) * 128, m0, bar_full + 8 * (i % stages));
@@ -276,31 +271,31 @@ __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_const
           xw[m][2] = v.z ^ 0x80808080u;
           xw[m][3] = v.w ^ 0x80808080u;
         }
+        // rows gr and gr + 8 of each n-tile, 16 bytes at k 64u + 16t (swizzled by the row)
+        uint4 wg[kW8WN], wg8[kW8WN];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4 cw[kW8WN];
+        for (int j = 0; j < kW8WN; ++j) {
+          const uint8_t* r0 = cs + ((warp * kW8WN + j) * 16 + gr) * 128 + (((4 * u + t) ^ gr) << 4);
+          wg[j] = *reinterpret_cast<const uint4*>(r0);
+          wg8[j] = *reinterpret_cast<const uint4*>(r0 + 8 * 128);
+        }
 #pragma unroll
-          for (int j = 0; j < kW8WN; ++j)
-            cw[j] = *reinterpret_cast<const uint4*>(cs + (((warp * kW8WN + j) * 2 + u) * 2 + h) * 512 + lane * 16);
+        for (int st = 0; st < 4; ++st) {
+          uint32_t a[kW8WN][4];
 #pragma unroll
-          for (int s2 = 0; s2 < 2; ++s2) {
-            const int st = 2 * h + s2;
-            uint32_t a[kW8WN][4];
+          for (int j = 0; j < kW8WN; ++j) {
+            const uint32_t w0 = st == 0 ? wg[j].x : st == 1 ? wg[j].y : st == 2 ? wg[j].z : wg[j].w;
+            const uint32_t w8 = st == 0 ? wg8[j].x : st == 1 ? wg8[j].y : st == 2 ? wg8[j].z : wg8[j].w;
+            a[j][0] = biased_to_half2(w0, 0);
+            a[j][1] = biased_to_half2(w8, 0);
+            a[j][2] = biased_to_half2(w0, 1);
+            a[j][3] = biased_to_half2(w8, 1);
+          }
 #pragma unroll
-            for (int j = 0; j < kW8WN; ++j) {
-              const uint32_t wg = s2 == 0 ? cw[j].x : cw[j].z;   // row gr
-              const uint32_t wg8 = s2 == 0 ? cw[j].y : cw[j].w;  // row gr + 8
-              a[j][0] = biased_to_half2(wg, 0);
-              a[j][1] = biased_to_half2(wg8, 0);
-              a[j][2] = biased_to_half2(wg, 1);
-              a[j][3] = biased_to_half2(wg8, 1);
-            }
+          for (int m = 0; m < MT; ++m) {
+            const uint32_t b0 = biased_to_half2(xw[m][st], 0), b1 = biased_to_half2(xw[m][st], 1);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t b0 = biased_to_half2(xw[m][st], 0), b1 = biased_to_half2(xw[m][st], 1);
-#pragma unroll
-              for (int j = 0; j < kW8WN; ++j) mma_16816(acc[j][m], a[j], b0, b1);
-            }
+            for (int j = 0; j < kW8WN; ++j) mma_16816(acc[j][m], a[j], b0, b1);
           }
         }
       }
@@ -385,8 +380,8 @@ uint32_t w8_smem(const W8Shape& g, int stages) {
 }
 
 template <int MT>
-tm_status w8_launch_t(const CUtensorMap& tmX, const W8Params& P, dim3 grid, int S, uint32_t smem,
-                      cudaStream_t stream) {
+tm_status w8_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8Params& P, dim3 grid, int S,
+                      uint32_t smem, cudaStream_t stream) {
   auto kern = w8_kernel<MT>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -413,7 +408,7 @@ tm_status w8_launch_t(const CUtensorMap& tmX, const W8Params& P, dim3 grid, int 
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, tmX, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
 }
 
 unsigned grid_1d(long long n, int block) { return (unsigned)((n + block - 1) / block); }
@@ -471,7 +466,7 @@ extern "C" tm_status tm_w8_pack(const int8_t* q, const float* sw, int K, int N, 
   p->NT = N / 16;
   p->KB = p->Kp / 128;
   p->device = dev;
-  const size_t code_bytes = (size_t)p->KB * p->NT * kW8Block;
+  const size_t code_bytes = (size_t)p->KB * N * 128;
   p->bytes = code_bytes + (size_t)N * 4;
   if (cudaMalloc(&p->base, p->bytes) != cudaSuccess) {
     delete p;
@@ -479,8 +474,22 @@ extern "C" tm_status tm_w8_pack(const int8_t* q, const float* sw, int K, int N, 
   }
   p->codes = static_cast<uint8_t*>(p->base);
   p->scales = reinterpret_cast<float*>(p->codes + code_bytes);
+  {
+    EncodeTiledFn fn = encode_tiled_fn();
+    cuuint64_t dims[3] = {128, (cuuint64_t)N, (cuuint64_t)p->KB};
+    cuuint64_t strides[2] = {128, (cuuint64_t)N * 128};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (!fn || fn(&p->tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, p->codes, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+      cudaFree(p->base);
+      delete p;
+      return TM_ERR_CUDA;
+    }
+  }
   const long long chunks = (long long)code_bytes / 16;
-  w8_pack_kernel<<<grid_1d(chunks, 256), 256>>>(q, K, N, p->NT, chunks, reinterpret_cast<uint4*>(p->codes));
+  w8_pack_kernel<<<grid_1d(chunks, 256), 256>>>(q, K, N, chunks, reinterpret_cast<uint4*>(p->codes));
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaMemcpy(p->scales, sw, (size_t)N * 4, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -495,7 +504,7 @@ extern "C" tm_status tm_w8_pack(const int8_t* q, const float* sw, int K, int N, 
 
 extern "C" tm_status tm_w8_unpack(const tm_w8_packed* p, int8_t* q, float* sw) {
   if (!p || !q || !sw) return TM_ERR_INVALID_ARG;
-  w8_unpack_kernel<<<grid_1d((long long)p->K * p->N, 256), 256>>>(p->codes, p->K, p->N, p->NT, q);
+  w8_unpack_kernel<<<grid_1d((long long)p->K * p->N, 256), 256>>>(p->codes, p->K, p->N, q);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaMemcpy(sw, p->scales, (size_t)p->N * 4, cudaMemcpyDeviceToDevice);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -581,10 +590,10 @@ extern "C" tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   tm_status res = TM_ERR_UNSUPPORTED;
   switch (MT) {
-    case 1: res = w8_launch_t<1>(tmX, P, grid, S, smem, st); break;
-    case 2: res = w8_launch_t<2>(tmX, P, grid, S, smem, st); break;
-    case 4: res = w8_launch_t<4>(tmX, P, grid, S, smem, st); break;
-    case 8: res = w8_launch_t<8>(tmX, P, grid, S, smem, st); break;
+    case 1: res = w8_launch_t<1>(tmX, p->tm_codes, P, grid, S, smem, st); break;
+    case 2: res = w8_launch_t<2>(tmX, p->tm_codes, P, grid, S, smem, st); break;
+    case 4: res = w8_launch_t<4>(tmX, p->tm_codes, P, grid, S, smem, st); break;
+    case 8: res = w8_launch_t<8>(tmX, p->tm_codes, P, grid, S, smem, st); break;
     default: break;
   }
   if (res == TM_OK) set_launch_count(1);
