@@ -70,7 +70,10 @@ void tm_w8_packed_free(tm_w8_packed* p);
  *   split_k: 0 automatic, else 1, 2, 4 or 8 CTAs (a thread-block cluster)
  *            sharing one output tile along K, reduced through distributed
  *            shared memory (no global workspace)
- * M up to 32 rows run in one row tile (decode), larger M in tiles of 64 rows.
+ * M up to 32 rows run on mma.sync in one row tile (decode); larger M on
+ * tcgen05 (kind::f16, fp32 accumulators in tensor memory) in tiles of 128
+ * output columns x 64 or 128 rows, both operands converted to exact fp16 in
+ * the kernel (weights into tensor memory, X into shared memory).
  * Waits are bounded: a copy that never lands sets the device timeout bit
  * (tm_device_error).
  */

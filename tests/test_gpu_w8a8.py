@@ -85,9 +85,18 @@ def test_pack_roundtrip(K, N):
     assert np.array_equal(sd.cpu().numpy().view(np.uint32), s.view(np.uint32))
 
 
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 32, 33, 64, 65, 130])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 17, 32, 33, 64, 65, 130, 300])
 def test_gemm_auto(M):
+    """M <= 32: the mma.sync kernel; above: the tensor-memory kernel (64- or 128-row tiles)."""
     _check(M, 1024, 512)
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("M", [40, 129])
+def test_gemm_tensor_memory_split_ragged(split, M):
+    """Cluster split along K with a partial last 128-k block, a partial 128-column
+    block (N = 272) and a partial row tile."""
+    _check(M, 1040, 272, split=split)
 
 
 def test_gemm_ragged_k_and_n():

@@ -360,6 +360,374 @@ __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------- tensor-memory W8A8 GEMM -----
+//
+// For larger M the products go to tcgen05 (kind::f16, fp32 accumulators in
+// tensor memory), both operands as exact fp16 integers:
+//   * warp 0, one thread: per 128-k block one TMA box of weight codes (128
+//     rows of W^T = the CTA's 128 output columns) and one of X (BT rows), both
+//     with the 128-byte swizzle, into a ring; weights of the first slots before
+//     `griddepcontrol.wait`, X after;
+//   * warps 2..9 convert a ring slot into one of two "converted" slots: the
+//     warp pair of tensor-memory lane quarter q turns rows 32q .. 32q+31 of the
+//     weight box (one 64-k unit each) into fp16 and writes them with
+//     tcgen05.st.32x32b as the MMA's A operand (lane = output column, column c
+//     = k pair c of a 16-k slice); all 256 threads turn the X box into fp16 rows
+//     of 128 bytes with the 128-byte swizzle (the K-major B operand), then
+//     release the ring slot;
+//   * warp 1, one thread: 8 MMAs (M = 128, N = BT, K = 16) per converted slot,
+//     whose commit frees it;
+//   * warps 2..9 again: epilogue, y = acc s_x[m] s_w[n] -> fp16; split K over a
+//     cluster reduces through distributed shared memory in rank order.
+constexpr int kW8TcThreads = 320;
+constexpr int kW8TcConv = 2;  // converted slots (tensor-memory A + fp16 X)
+
+template <int BT>
+struct W8TcShape {
+  static constexpr uint32_t W_BYTES = 128 * 128;  // one 128-k block of 128 weight rows
+  static constexpr uint32_t XR_BYTES = BT * 128;  // one 128-k block of BT int8 rows
+  static constexpr uint32_t SLOT = W_BYTES + XR_BYTES;
+  static constexpr uint32_t XF_UNIT = BT * 128;  // fp16 X, one 64-k unit
+  static constexpr uint32_t XF_SLOT = 2 * XF_UNIT;
+  static constexpr uint32_t A_COLS = 64;  // 8 slices of 16 k, 8 columns each
+  static constexpr uint32_t A_COL = BT;   // A slots right after the accumulator columns
+  static constexpr uint32_t TMEM_COLS = BT + kW8TcConv * A_COLS <= 256 ? 256 : 512;
+  static constexpr int TPR = 256 / BT;     // converter threads per X row
+  static constexpr int CPT = 8 / TPR;      // 16-byte X chunks per converter thread
+  static_assert(SLOT % 1024 == 0 && XF_UNIT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+};
+
+struct W8TcParams {
+  const float* sw;
+  const float* sx;
+  __half* Y;
+  int M, N;
+  int kb_total, kb_per_cta;
+  int stages;       // ring slots
+  uint32_t xf_off;  // offset of the converted X slots
+  uint32_t bar_off;
+};
+
+__device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
+}
+
+template <int BT>
+__global__ void __launch_bounds__(kW8TcThreads, 1)
+    w8tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const W8TcParams P) {
+  using SH = W8TcShape<BT>;
+  constexpr int SC = kW8TcConv;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt0 = blockIdx.x * 8;
+  const int m0 = blockIdx.y * BT;
+  const int S = gridDim.z;
+  const int kb0 = blockIdx.z * P.kb_per_cta;
+  const int nkb = max(0, min(P.kb_total, kb0 + P.kb_per_cta) - kb0);
+  const int SA = P.stages;
+
+  const uint32_t barA = base + P.bar_off;  // [SA] full, then [SA] empty
+  const uint32_t barC = barA + 16 * SA;    // [SC] full, then [SC] empty (converted slots)
+  const uint32_t bar_acc = barC + 16 * SC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.bar_off + 16 * SA + 16 * SC + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + 16 * SA + 16 * SC + 12);
+  auto fullA = [&](int s) { return barA + 8 * s; };
+  auto emptyA = [&](int s) { return barA + 8 * (SA + s); };
+  auto fullC = [&](int s) { return barC + 8 * s; };
+  auto emptyC = [&](int s) { return barC + 8 * (SC + s); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(fullA(s), 1);
+      mbar_init(emptyA(s), 8);
+    }
+    for (int s = 0; s < SC; ++s) {
+      mbar_init(fullC(s), 8);
+      mbar_init(emptyC(s), 1);
+    }
+    mbar_init(bar_acc, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    launch_dependents();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), SH::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // D at columns 0 .. BT-1, A slots from A_COL
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmW);
+      auto issue_w = [&](int i, int s) { tma_load_3d(base + s * SH::SLOT, &tmW, 0, nt0 * 16, kb0 + i, fullA(s)); };
+      auto issue_x = [&](int i, int s) {
+        tma_load_2d(base + s * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(s));
+      };
+      const int first = min(nkb, SA);
+      for (int i = 0; i < first; ++i) {
+        mbar_expect_tx(fullA(i), SH::SLOT);
+        issue_w(i, i);
+      }
+      grid_dependency_wait();
+      for (int i = 0; i < first; ++i) issue_x(i, i);
+      int issued = first;
+      for (int i = first; i < nkb; ++i) {
+        const int s = i % SA;
+        if (!mbar_wait(emptyA(s), (uint32_t)(i / SA - 1) & 1u, abort_flag, &s_err_w8)) break;
+        mbar_expect_tx(fullA(s), SH::SLOT);
+        issue_w(i, s);
+        issue_x(i, s);
+        issued = i + 1;
+      }
+      // never leave with copies in flight into this CTA's shared memory
+      for (int i = max(0, issued - SA); i < issued; ++i) w8_drain(fullA(i % SA), (uint32_t)(i / SA) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(128, BT);
+      for (int i = 0; i < nkb; ++i) {
+        const int sc = i % SC;
+        if (!mbar_wait(fullC(sc), (uint32_t)(i / SC) & 1u, abort_flag, &s_err_w8)) break;
+        tc_fence_after();
+        const uint64_t db = smem_desc_sw128(base + P.xf_off + sc * SH::XF_SLOT);
+        const uint32_t ta = tmem + SH::A_COL + SH::A_COLS * sc;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc_mma_f16_ta(tmem, ta + 8u * (4 * u + k), db + (uint64_t)((u * SH::XF_UNIT) >> 4) + (uint64_t)(2 * k),
+                          idesc, (i > 0 || u > 0 || k > 0) ? 1u : 0u);
+        tc_commit(emptyC(sc));
+      }
+      // completes once every MMA issued above has finished (also on abort)
+      tc_commit(bar_acc);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- converters: warps 2..9 ----------------
+    const int cw = warp - 2;
+    const int q = warp & 3;    // tensor-memory lane quarter of this warp
+    const int hu = cw >> 2;    // its 64-k unit of the weight block
+    const int wrow = 32 * q + lane;
+    const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+    const int T = cw * 32 + lane;
+    const int xr = T / SH::TPR, part = T % SH::TPR;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % SA, sc = i % SC;
+      if (!mbar_wait(fullA(s), (uint32_t)(i / SA) & 1u, abort_flag, &s_err_w8)) break;
+      if (!mbar_wait(emptyC(sc), ((uint32_t)(i / SC) & 1u) ^ 1u, abort_flag, &s_err_w8)) break;
+      tc_fence_after();
+      const uint32_t st = base + s * SH::SLOT;
+      // weights: row wrow, k 64 hu + 16 s4 .. +15 -> 8 columns of slice 4 hu + s4
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const uint4 v = lds128(st + wrow * 128 + (((4 * hu + s4) ^ (wrow & 7)) << 4));
+        const uint32_t r[8] = {biased_to_half2(v.x, 0), biased_to_half2(v.x, 1), biased_to_half2(v.y, 0),
+                               biased_to_half2(v.y, 1), biased_to_half2(v.z, 0), biased_to_half2(v.z, 1),
+                               biased_to_half2(v.w, 0), biased_to_half2(v.w, 1)};
+        tc_st_32x32b_x8(tmem + t_lane + SH::A_COL + SH::A_COLS * sc + 8u * (4 * hu + s4), r);
+      }
+      // X: row xr, chunks part * CPT .. +CPT-1 (16 k each) -> fp16, 128-byte swizzle
+      const uint32_t xin = st + SH::W_BYTES + xr * 128;
+      const uint32_t xout = base + P.xf_off + sc * SH::XF_SLOT + xr * 128;
+#pragma unroll
+      for (int c2 = 0; c2 < SH::CPT; ++c2) {
+        const int c = part * SH::CPT + c2;
+        const uint4 v = lds128(xin + ((c ^ (xr & 7)) << 4));
+        const uint32_t w0 = v.x ^ 0x80808080u, w1 = v.y ^ 0x80808080u, w2 = v.z ^ 0x80808080u,
+                       w3 = v.w ^ 0x80808080u;
+        const uint32_t o = xout + (c >> 2) * SH::XF_UNIT;
+        const int oc = 2 * (c & 3);
+        sts128(o + ((oc ^ (xr & 7)) << 4), biased_to_half2(w0, 0), biased_to_half2(w0, 1), biased_to_half2(w1, 0),
+               biased_to_half2(w1, 1));
+        sts128(o + (((oc + 1) ^ (xr & 7)) << 4), biased_to_half2(w2, 0), biased_to_half2(w2, 1),
+               biased_to_half2(w3, 0), biased_to_half2(w3, 1));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      fence_proxy_async_smem();  // the fp16 X tile is read by the tensor core (async proxy)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(fullC(sc));
+        mbar_arrive(emptyA(s));
+      }
+    }
+  }
+
+  // ---------------- epilogue: warps 2..9, TMEM lanes 32 q .. 32 q + 31 ----------------
+  const bool epi = warp >= 2;
+  const int q = warp & 3;
+  const int h = (warp - 2) >> 2;
+  const int row = 32 * q + lane;  // output column within the CTA (TMEM lane)
+  constexpr int HALF = BT / 2;    // token columns per epilogue warp
+  bool acc_ok = true;
+  if (epi) {
+    acc_ok = mbar_wait(bar_acc, 0, abort_flag, &s_err_w8);
+    acc_ok = __all_sync(0xffffffffu, acc_ok);
+    tc_fence_after();
+  }
+  if (S == 1) {
+    if (epi) grid_dependency_wait();  // Y may still be read by the preceding grid
+    if (epi && acc_ok) {
+      const int n = nt0 * 16 + row;
+      const float swn = n < P.N ? P.sw[n] : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < HALF; c += 8) {
+        uint32_t v[8];
+        tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c), v);
+        tc_wait_ld();
+        if (n < P.N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int m = m0 + h * HALF + c + e;
+            if (m < P.M) P.Y[(size_t)m * P.N + n] = __float2half_rn(__uint_as_float(v[e]) * P.sx[m] * swn);
+          }
+        }
+      }
+    }
+  } else {
+    // Split K: every CTA's ring is idle once all of the cluster passes this
+    // barrier (MMAs finished, copies drained), so partial tiles may land there.
+    cluster_sync_all();
+    const int R = 128 / S;  // output columns owned by each rank
+    const uint32_t my_rank = cluster_ctarank();
+    if (epi) {
+      const int owner = row / R, rr = row - owner * R;
+      const uint32_t dst = map_shared_rank(base + (uint32_t)(((int)my_rank * R + rr) * BT) * 4u, (uint32_t)owner);
+#pragma unroll 1
+      for (int c = 0; c < HALF; c += 8) {
+        uint32_t v[8];
+        if (acc_ok && nkb > 0) {  // a CTA with no K blocks contributes zeros
+          tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c), v);
+          tc_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = 0u;
+        }
+        const uint32_t d = dst + (uint32_t)(h * HALF + c) * 4u;
+        st_dsmem_v4(d, v[0], v[1], v[2], v[3]);
+        st_dsmem_v4(d + 16, v[4], v[5], v[6], v[7]);
+      }
+    }
+    cluster_sync_all();
+    grid_dependency_wait();
+    const float* red = reinterpret_cast<const float*>(smem);
+    const int n_base = nt0 * 16 + (int)my_rank * R;
+    for (int it = threadIdx.x; it < R * BT; it += blockDim.x) {
+      const int tok = it / R, rr = it - tok * R;
+      const int m = m0 + tok, n = n_base + rr;
+      if (m >= P.M || n >= P.N) continue;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < S; ++k) acc += red[(k * R + rr) * BT + tok];
+      P.Y[(size_t)m * P.N + n] = __float2half_rn(acc * P.sx[m] * P.sw[n]);
+    }
+  }
+  if (warp == 1 && lane == 0) w8_drain(bar_acc, 0);  // no MMA may still run when TMEM is released
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, SH::TMEM_COLS);
+  }
+}
+
+template <int BT>
+tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8TcParams& P, dim3 grid, int S,
+                        uint32_t smem, cudaStream_t stream) {
+  auto kern = w8tc_kernel<BT>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW8SmemMax) != cudaSuccess)
+      return TM_ERR_CUDA;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kW8TcThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (S > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = 1;
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = (unsigned)S;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+}
+
+// Shared memory of the tensor-memory kernel: ring, converted X slots, barriers, alignment slack.
+template <int BT>
+uint32_t w8tc_smem(int stages) {
+  using SH = W8TcShape<BT>;
+  return stages * SH::SLOT + kW8TcConv * SH::XF_SLOT + 16 * stages + 16 * kW8TcConv + 16 + 1024;
+}
+
+template <int BT>
+tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
+                   cudaStream_t stream) {
+  using SH = W8TcShape<BT>;
+  const int NB = (p->NT + 7) / 8, MB = (M + BT - 1) / BT;
+  const int sms = num_sms(p->device);
+  int S = split_k;
+  if (!S) {
+    // split K (a cluster) while the tiles fill fewer than half the SMs and
+    // each CTA keeps at least two 128-k blocks
+    S = 1;
+    while (S < 4 && (long long)NB * MB * S * 2 <= sms && p->KB / (2 * S) >= 2) S *= 2;
+  }
+  int stages = 8;
+  while (stages > 2 && w8tc_smem<BT>(stages) > kW8SmemMax) --stages;
+  const uint32_t smem = w8tc_smem<BT>(stages);
+  if (smem > kW8SmemMax) return TM_ERR_UNSUPPORTED;
+  CUtensorMap tmX;
+  {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return TM_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)p->K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)p->K};
+    cuuint32_t box[2] = {128, (cuuint32_t)BT};
+    cuuint32_t es[2] = {1, 1};
+    if (fn(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(xq), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TM_ERR_CUDA;
+  }
+  W8TcParams P;
+  P.sw = p->scales;
+  P.sx = sx;
+  P.Y = reinterpret_cast<__half*>(Y);
+  P.M = M;
+  P.N = p->N;
+  P.kb_total = p->KB;
+  P.kb_per_cta = (p->KB + S - 1) / S;
+  P.stages = stages;
+  P.xf_off = stages * SH::SLOT;
+  P.bar_off = P.xf_off + kW8TcConv * SH::XF_SLOT;
+  return w8tc_launch_t<BT>(tmX, p->tm_codes, P, dim3((unsigned)NB, (unsigned)MB, (unsigned)S), S, smem, stream);
+}
+
 int w8_mt(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
 
 struct W8Shape {
@@ -533,6 +901,12 @@ extern "C" tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8
       (reinterpret_cast<uintptr_t>(sx) & 3u))
     return TM_ERR_ALIGNMENT;
   if (M == 0) return TM_OK;
+  if (M > 32) {
+    const tm_status r = M <= 64 ? w8tc_run<64>(xq, sx, p, Y, M, split_k, reinterpret_cast<cudaStream_t>(stream))
+                                : w8tc_run<128>(xq, sx, p, Y, M, split_k, reinterpret_cast<cudaStream_t>(stream));
+    if (r == TM_OK) set_launch_count(1);
+    return r;
+  }
   const int MT = w8_mt(M);
   const int MB = (M + 8 * MT - 1) / (8 * MT);
   const int NB = (p->NT + kW8CN - 1) / kW8CN;
