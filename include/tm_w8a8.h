@@ -80,6 +80,11 @@ void tm_w8_packed_free(tm_w8_packed* p);
 tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
                        void* stream);
 
+/* tm_w8a8_gemm with the rows of X per CTA of the tensor-memory kernel (M > 32)
+ * chosen explicitly: tile_m = 64, 128 or 256 (0 = automatic; ignored for M <= 32). */
+tm_status tm_w8a8_gemm_ex(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
+                          int tile_m, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

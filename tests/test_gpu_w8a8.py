@@ -47,11 +47,12 @@ def _acts(M, K, tag="x"):
     return X
 
 
-def _check(M, K, N, split=0, rows=None):
+def _check(M, K, N, split=0, rows=None, tile_m=0):
     q, s = _weights(K, N)
     X = _acts(M, K)
     qx, sx = w8.quantize_act(X)
-    Y = binding.w8a8_gemm(torch.from_numpy(qx).cuda(), torch.from_numpy(sx).cuda(), _packed(K, N), split=split)
+    Y = binding.w8a8_gemm(torch.from_numpy(qx).cuda(), torch.from_numpy(sx).cuda(), _packed(K, N), split=split,
+                          tile_m=tile_m)
     torch.cuda.synchronize()
     assert binding.device_error(clear=True) == 0
     rows = sample_rows(M) if rows is None else rows
@@ -91,12 +92,14 @@ def test_gemm_auto(M):
     _check(M, 1024, 512)
 
 
-@pytest.mark.parametrize("split", [2, 4, 8])
-@pytest.mark.parametrize("M", [40, 129])
-def test_gemm_tensor_memory_split_ragged(split, M):
-    """Cluster split along K with a partial last 128-k block, a partial 128-column
-    block (N = 272) and a partial row tile."""
-    _check(M, 1040, 272, split=split)
+@pytest.mark.parametrize("tile_m", [64, 128, 256])
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [40, 129, 300])
+def test_gemm_tensor_memory_tiles_split_ragged(tile_m, split, M):
+    """Every row tile and cluster split of the tensor-memory kernel on a partial
+    last 128-k block (K = 1040), a partial 128-column block (N = 272) and a
+    partial row tile."""
+    _check(M, 1040, 272, split=split, tile_m=tile_m)
 
 
 def test_gemm_ragged_k_and_n():

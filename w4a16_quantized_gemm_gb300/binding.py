@@ -23,7 +23,7 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
-           "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm")
+           "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex")
 
 
 class TMError(RuntimeError):
@@ -105,6 +105,8 @@ def load(path: Optional[str] = None):
     lib.tm_w8_packed_free.argtypes = [vp]
     lib.tm_w8a8_gemm.restype = ci
     lib.tm_w8a8_gemm.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+    lib.tm_w8a8_gemm_ex.restype = ci
+    lib.tm_w8a8_gemm_ex.argtypes = [vp, vp, vp, vp, ci, ci, ci, vp]
     _lib = lib
     return lib
 
@@ -423,8 +425,8 @@ def pack_w8(q: torch.Tensor, sw: torch.Tensor) -> W8Packed:
 
 
 def w8a8_gemm(xq: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[torch.Tensor] = None, split: int = 0,
-              stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Y = fp16(sx sw^T (xq . q_w)) for int8 xq [M][K] and fp32 sx [M] (tm_w8a8_gemm)."""
+              tile_m: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Y = fp16(sx sw^T (xq . q_w)) for int8 xq [M][K] and fp32 sx [M] (tm_w8a8_gemm_ex)."""
     if xq.dim() != 2 or xq.shape[1] != w.K:
         raise ValueError("xq must be int8 [M][K]")
     M = xq.shape[0]
@@ -433,7 +435,7 @@ def w8a8_gemm(xq: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[tor
     if tuple(out.shape) != (M, w.N):
         raise ValueError("out must be fp16 [M][N]")
     st = stream if stream is not None else torch.cuda.current_stream(xq.device)
-    _check(load().tm_w8a8_gemm(_dev(xq, torch.int8, "xq"), _dev(sx, torch.float32, "sx"), w.handle,
-                               _dev(out, torch.float16, "out"), M, split, ctypes.c_void_p(st.cuda_stream)),
-           "tm_w8a8_gemm")
+    _check(load().tm_w8a8_gemm_ex(_dev(xq, torch.int8, "xq"), _dev(sx, torch.float32, "sx"), w.handle,
+                                  _dev(out, torch.float16, "out"), M, split, tile_m, ctypes.c_void_p(st.cuda_stream)),
+           "tm_w8a8_gemm_ex")
     return out

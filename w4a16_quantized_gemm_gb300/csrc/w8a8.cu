@@ -692,10 +692,10 @@ tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, voi
   const int sms = num_sms(p->device);
   int S = split_k;
   if (!S) {
-    // split K (a cluster) while the tiles fill fewer than half the SMs and
-    // each CTA keeps at least two 128-k blocks
+    // split K (a cluster) while the doubled grid still fits in one wave (one
+    // CTA per SM) and each CTA keeps at least two 128-k blocks
     S = 1;
-    while (S < 4 && (long long)NB * MB * S * 2 <= sms && p->KB / (2 * S) >= 2) S *= 2;
+    while (S < 8 && (long long)NB * MB * S * 2 <= sms && p->KB / (2 * S) >= 2) S *= 2;
   }
   int stages = 8;
   while (stages > 2 && w8tc_smem<BT>(stages) > kW8SmemMax) --stages;
@@ -729,6 +729,28 @@ tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, voi
 }
 
 int w8_mt(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
+
+// Rows of X per CTA for the tensor-memory kernel: the tile size with the
+// smallest estimated time, waves x (rows / relative MMA efficiency) -- an MMA
+// of N = 128 costs about as much to issue as its tensor time, so 128-row tiles
+// run at roughly 0.55 of the 256-row rate; 64 rows only for M <= 64.
+int w8tc_rows(int M, int NT, int sms) {
+  if (M <= 64) return 64;
+  const int NB = (NT + 7) / 8;
+  const double eff[2] = {0.55, 1.0};
+  const int rows[2] = {128, 256};
+  int best = 128;
+  double best_t = 1e30;
+  for (int i = 0; i < 2; ++i) {
+    const long long tiles = (long long)NB * ((M + rows[i] - 1) / rows[i]);
+    const double t = (double)((tiles + sms - 1) / sms) * rows[i] / eff[i];
+    if (t < best_t) {
+      best_t = t;
+      best = rows[i];
+    }
+  }
+  return best;
+}
 
 struct W8Shape {
   uint32_t x_bytes, stage, red;
@@ -893,17 +915,21 @@ extern "C" void tm_w8_packed_free(tm_w8_packed* p) {
   delete p;
 }
 
-extern "C" tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M,
-                                  int split_k, void* stream) {
+extern "C" tm_status tm_w8a8_gemm_ex(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M,
+                                     int split_k, int tile_m, void* stream) {
   if (!xq || !sx || !p || !Y || M < 0) return TM_ERR_INVALID_ARG;
   if (split_k < 0 || split_k > 8 || (split_k & (split_k - 1))) return TM_ERR_INVALID_ARG;
+  if (tile_m != 0 && tile_m != 64 && tile_m != 128 && tile_m != 256) return TM_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(xq) & 15u) || (reinterpret_cast<uintptr_t>(Y) & 15u) ||
       (reinterpret_cast<uintptr_t>(sx) & 3u))
     return TM_ERR_ALIGNMENT;
   if (M == 0) return TM_OK;
   if (M > 32) {
-    const tm_status r = M <= 64 ? w8tc_run<64>(xq, sx, p, Y, M, split_k, reinterpret_cast<cudaStream_t>(stream))
-                                : w8tc_run<128>(xq, sx, p, Y, M, split_k, reinterpret_cast<cudaStream_t>(stream));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int BT = tile_m ? tile_m : w8tc_rows(M, p->NT, num_sms(p->device));
+    const tm_status r = BT == 64    ? w8tc_run<64>(xq, sx, p, Y, M, split_k, st)
+                        : BT == 128 ? w8tc_run<128>(xq, sx, p, Y, M, split_k, st)
+                                    : w8tc_run<256>(xq, sx, p, Y, M, split_k, st);
     if (r == TM_OK) set_launch_count(1);
     return r;
   }
@@ -972,4 +998,9 @@ extern "C" tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8
   }
   if (res == TM_OK) set_launch_count(1);
   return res;
+}
+
+extern "C" tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M,
+                                  int split_k, void* stream) {
+  return tm_w8a8_gemm_ex(xq, sx, p, Y, M, split_k, 0, stream);
 }
