@@ -425,8 +425,10 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
   uint8_t* smem = smem_raw + (base - raw_base);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt0 = blockIdx.x * 8;
-  const int m0 = blockIdx.y * BT;
+  // row blocks vary fastest: the CTAs that share a weight tile run together
+  // and read it from L2
+  const int m0 = blockIdx.x * BT;
+  const int nt0 = blockIdx.y * 8;
   const int S = gridDim.z;
   const int kb0 = blockIdx.z * P.kb_per_cta;
   const int nkb = max(0, min(P.kb_total, kb0 + P.kb_per_cta) - kb0);
@@ -725,7 +727,7 @@ tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, voi
   P.stages = stages;
   P.xf_off = stages * SH::SLOT;
   P.bar_off = P.xf_off + kW8TcConv * SH::XF_SLOT;
-  return w8tc_launch_t<BT>(tmX, p->tm_codes, P, dim3((unsigned)NB, (unsigned)MB, (unsigned)S), S, smem, stream);
+  return w8tc_launch_t<BT>(tmX, p->tm_codes, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem, stream);
 }
 
 int w8_mt(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
