@@ -943,8 +943,10 @@ def run_w8a8(args, rank, world, local, prefill=False):
                    "launches_per_step": 2 * len(items), "bytes_per_step": step_bytes, "flops_per_step": step_flops,
                    "l2": f"each GEMM has its own packed weights ({weight_bytes / 1e6:.0f} MB per step > 129 MB L2)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peaks["source"],
-                     "kernel": "w8_kernel (+ w8_quant_act_kernel), whole step"},
+                     "frac": round(achieved / peak, 4),
+                     "traffic": None if prefill else read_traffic("w8", "llama3_8b_w8a8"),
+                     "peak_source": peaks["source"], "kernel": "w8tc_kernel (+ w8_quant_act_kernel), whole step"
+                     if prefill else "w8_kernel (+ w8_quant_act_kernel), whole step"},
         "gpu_launches": 2 * len(items) * args.steps, "clocks": clocks, "cpu_baseline": cpu,
     }
     if rank == 0:

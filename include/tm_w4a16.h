@@ -127,12 +127,13 @@ tm_status tm_kv_quantize(const uint16_t* X, long long rows, int D, int bits, uin
  * Value codes of the head-major cache, [B][Hkv][L][D*bits/8] with D = 128 (as
  * tm_kv_quantize writes them for vectors ordered (sequence, KV head, token)),
  * to the tiles tm_kv_decode_attention reads: [B][Hkv][L/16][16*D*bits/8],
- * each 16-token tile in MMA lane order -- 16-byte chunk (c, lane = 4 gr + t)
- * holds, for the n8 blocks j of chunk c, the codes of dimension 8 j + gr for
- * tokens 4t .. 4t+3 (int8: 4 chunks of 4 blocks, a byte per token; int4: 2
- * chunks of 8 blocks, 16 bits per block, tokens 4t, 4t+1 in the low and high
- * nibble of the first byte).  L % 16 == 0; tiles 16-byte aligned.
- * Asynchronous on `stream`, one launch.
+ * each 16-token tile in MMA A-fragment order, 16-byte chunk (c, lane = 4 gr + t):
+ * int8 -- 4 chunks, word k of chunk c holds the codes of dimension
+ * 8(4c + k) + gr for tokens 2t, 2t+1, 2t+8, 2t+9 (a byte each); int4 -- 2
+ * chunks, word k of chunk c belongs to MMA p = 4c + k, its nibbles 0..7 being
+ * (token, dimension) (2t, A), (2t+8, A), (2t, B), (2t+8, B), (2t+1, A),
+ * (2t+9, A), (2t+1, B), (2t+9, B) with A = 16p + gr, B = A + 8.  L % 16 == 0;
+ * tiles 16-byte aligned.  Asynchronous on `stream`, one launch.
  */
 tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, uint8_t* tiles, void* stream);
 

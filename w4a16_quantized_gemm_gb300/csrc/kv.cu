@@ -224,41 +224,31 @@ __device__ __forceinline__ void finish_attention(const float* part, float* cta, 
 //     dimensions without the factor 16, 64 times the rest), removed with the
 //     zero point afterwards: score = s_k (Q . c - z_k sum Q) / sqrt(D), in
 //     fp32, kept in units of log2 (the softmax uses powers of two).  The k
-//     order is permuted the same way on K and Q: in slice sl the slots 2t,
-//     2t+1, 2t+8, 2t+9 of lane t hold dimensions 32t + 4sl .. 32t + 4sl + 3, so
-//     a lane reads the 32 dimensions it needs of a token with two (int8) or
-//     one (int4) 16-byte loads.
+//     order is permuted the same way on K and Q so that a lane reads the 32
+//     dimensions 32t .. 32t+31 it needs of a token with two (int8) or one
+//     (int4) 16-byte loads: in slice sl the slots 2t, 2t+1, 2t+8, 2t+9 of lane
+//     t hold dimensions 32t + 4sl + (0, 1, 2, 3) for int8 -- one byte-permute
+//     per pair -- and 32t + 8(sl/2) + (0, 4, 1, 5) or (2, 6, 3, 7) for int4,
+//     so that one mask-and-OR per pair takes the nibbles straight out of a
+//     32-bit word.
 //   out^T [128 dims x 8 heads] += V codes^T . P', 8 MMAs: P' = p s_v (rounded
 //     once to fp16) is the score fragment transposed by two movmatrix; the
 //     value tile holds, per lane, the codes of dimensions 8q + gr (q = 0..15)
-//     for tokens 2t, 2t+1, 2t+8, 2t+9 in MMA A-fragment order.  The value
+//     for tokens 2t, 2t+1, 2t+8, 2t+9 in MMA A-fragment order (int4: one
+//     32-bit word per MMA, the four pairs taken out by masks).  The value
 //     zero point is removed once per head at the end (sum_t P'_t z_t).
 // A lane (gr, t) owns query heads 2t and 2t+1 throughout: after the max over
 // the tile's tokens (three shuffles) the online softmax is lane-local.
 
-// Two codes -> two exact fp16 values.  int8: bytes 2i, 2i+1 of w; int4: the
-// low and high nibble of byte i of w.
-template <int BITS>
+// Two int8 codes (bytes 2i, 2i+1 of w) -> two exact fp16 values.
 __device__ __forceinline__ uint32_t codes_to_half2(uint32_t w, int i) {
-  if constexpr (BITS == 8) {
-    const uint32_t x = __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);  // (1024 + c0, 1024 + c1)
-    return hsub2_u32(x, 0x64006400u);
-  } else {
-    const uint32_t x = __byte_perm(w, 0u, 0x4040u | (uint32_t)i | ((uint32_t)i << 8));  // byte i in bytes 0 and 2
-    const uint32_t y = lop3<0xEA>(x, 0x00F0000Fu, 0x64006400u);  // (1024 + lo, 1024 + 16 hi)
-    return hfma2_u32(y, 0x2C003C00u, 0xD400E400u);              // (x - 1024, x / 16 - 64)
-  }
+  const uint32_t x = __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);  // (1024 + c0, 1024 + c1)
+  return hsub2_u32(x, 0x64006400u);
 }
 
-// Raw form of the key codes for the score MMA: int8 bytes 2i, 2i+1 of w ->
-// (1024 + c0, 1024 + c1); int4 byte i -> (1024 + lo, 1024 + 16 hi).
-template <int BITS>
+// Raw form of two int8 key codes for the score MMA: (1024 + c0, 1024 + c1).
 __device__ __forceinline__ uint32_t codes_raw(uint32_t w, int i) {
-  if constexpr (BITS == 8) {
-    return __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);
-  } else {
-    return lop3<0xEA>(__byte_perm(w, 0u, 0x4040u | (uint32_t)i | ((uint32_t)i << 8)), 0x00F0000Fu, 0x64006400u);
-  }
+  return __byte_perm(w, 0x6464u, i == 0 ? 0x4140u : 0x4342u);
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
@@ -360,12 +350,20 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
         qe += f.x;
         qo += f.y;
-        if constexpr (BITS == 4) wv[e] = hmul2_u32(wv[e], 0x2C003C00u);  // (x, y / 16), exact
       }
-      qb[2 * c][0] = wv[0];
-      qb[2 * c][1] = wv[1];
-      qb[2 * c + 1][0] = wv[2];
-      qb[2 * c + 1][1] = wv[3];
+      if constexpr (BITS == 8) {
+        qb[2 * c][0] = wv[0];
+        qb[2 * c][1] = wv[1];
+        qb[2 * c + 1][0] = wv[2];
+        qb[2 * c + 1][1] = wv[3];
+      } else {
+        // dimensions 8c + i of the lane's 32: slice 2c pairs (0, 4) and (1, 5),
+        // slice 2c + 1 pairs (2, 6) and (3, 7); odd dimensions / 16 (exact)
+        qb[2 * c][0] = __byte_perm(wv[0], wv[2], 0x5410u);
+        qb[2 * c][1] = hmul2_u32(__byte_perm(wv[0], wv[2], 0x7632u), 0x2C002C00u);
+        qb[2 * c + 1][0] = __byte_perm(wv[1], wv[3], 0x5410u);
+        qb[2 * c + 1][1] = hmul2_u32(__byte_perm(wv[1], wv[3], 0x7632u), 0x2C002C00u);
+      }
     }
 #pragma unroll
     for (int x = 1; x <= 2; x <<= 1) {
@@ -421,16 +419,20 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       for (int sl = 0; sl < 8; ++sl) {
         uint32_t a[4];
         if constexpr (BITS == 8) {
-          a[0] = codes_raw<8>(wa[sl], 0);
-          a[1] = codes_raw<8>(wb[sl], 0);
-          a[2] = codes_raw<8>(wa[sl], 1);
-          a[3] = codes_raw<8>(wb[sl], 1);
+          a[0] = codes_raw(wa[sl], 0);
+          a[1] = codes_raw(wb[sl], 0);
+          a[2] = codes_raw(wa[sl], 1);
+          a[3] = codes_raw(wb[sl], 1);
         } else {
-          const int by = 2 * (sl & 1);
-          a[0] = codes_raw<4>(wa[sl >> 1], by);
-          a[1] = codes_raw<4>(wb[sl >> 1], by);
-          a[2] = codes_raw<4>(wa[sl >> 1], by + 1);
-          a[3] = codes_raw<4>(wb[sl >> 1], by + 1);
+          // word sl/2 holds dimensions 0..7 as nibbles 0..7: the low nibbles of
+          // bytes 0 and 2 are dimensions 0 and 4, the high ones 1 and 5 (x 16);
+          // shifted by a byte, 2 and 6, 3 and 7
+          const uint32_t xa = (sl & 1) ? wa[sl >> 1] >> 8 : wa[sl >> 1];
+          const uint32_t xb = (sl & 1) ? wb[sl >> 1] >> 8 : wb[sl >> 1];
+          a[0] = lop3<0xEA>(xa, 0x000F000Fu, 0x64006400u);
+          a[1] = lop3<0xEA>(xb, 0x000F000Fu, 0x64006400u);
+          a[2] = lop3<0xEA>(xa, 0x00F000F0u, 0x64006400u);
+          a[3] = lop3<0xEA>(xb, 0x00F000F0u, 0x64006400u);
         }
         mma_16816((sl & 1) ? d1 : d0, a, qb[sl][0], qb[sl][1]);
       }
@@ -496,15 +498,18 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       for (int p = 0; p < 8; ++p) {
         uint32_t a[4];
         if constexpr (BITS == 8) {
-          a[0] = codes_to_half2<8>(vw[2 * p], 0);
-          a[1] = codes_to_half2<8>(vw[2 * p + 1], 0);
-          a[2] = codes_to_half2<8>(vw[2 * p], 1);
-          a[3] = codes_to_half2<8>(vw[2 * p + 1], 1);
+          a[0] = codes_to_half2(vw[2 * p], 0);
+          a[1] = codes_to_half2(vw[2 * p + 1], 0);
+          a[2] = codes_to_half2(vw[2 * p], 1);
+          a[3] = codes_to_half2(vw[2 * p + 1], 1);
         } else {
-          a[0] = codes_to_half2<4>(vw[p], 0);
-          a[1] = codes_to_half2<4>(vw[p], 2);
-          a[2] = codes_to_half2<4>(vw[p], 1);
-          a[3] = codes_to_half2<4>(vw[p], 3);
+          // nibbles: 0 / 4 tokens 2t / 2t+1 of dimension 16p + gr, 1 / 5 tokens
+          // 2t+8 / 2t+9; shifted by a byte, the same for dimension 16p + 8 + gr
+          const uint32_t w = vw[p], w8 = w >> 8;
+          a[0] = hsub2_u32(lop3<0xEA>(w, 0x000F000Fu, 0x64006400u), 0x64006400u);
+          a[1] = hsub2_u32(lop3<0xEA>(w8, 0x000F000Fu, 0x64006400u), 0x64006400u);
+          a[2] = hfma2_u32(lop3<0xEA>(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
+          a[3] = hfma2_u32(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
         }
         mma_16816(o[p], a, pb0, pb1);
       }
@@ -542,11 +547,12 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
 }
 
 // Value codes [B][Hkv][L][D * BITS / 8] -> tiles [B][Hkv][L / 16][16 * D *
-// BITS / 8] in the kernel's A-fragment order: 16-byte chunk (c, lane = 4 gr +
-// t) holds, for q of chunk c, the codes of dimension 8q + gr for tokens 2t,
-// 2t+1, 2t+8, 2t+9 -- int8: 4 chunks of 4 q, one byte per token; int4: 2
-// chunks of 8 q, 16 bits per q (tokens 2t, 2t+1 in the low and high nibble of
-// the first byte, 2t+8, 2t+9 in the second).
+// BITS / 8] in the kernel's A-fragment order, 16-byte chunk (c, lane = 4 gr +
+// t): int8 -- 4 chunks; word k of chunk c holds the codes of dimension
+// 8(4c + k) + gr for tokens 2t, 2t+1, 2t+8, 2t+9, one byte each; int4 -- 2
+// chunks; word k of chunk c is MMA p = 4c + k, nibbles 0..7 = (token, dimension)
+// (2t, A), (2t+8, A), (2t, B), (2t+8, B), (2t+1, A), (2t+9, A), (2t+1, B),
+// (2t+9, B) with A = 16p + gr, B = A + 8.
 template <int BITS>
 __global__ void kv_pack_v_kernel(const uint8_t* __restrict__ codes, int B, int L, int Hkv,
                                  uint8_t* __restrict__ tiles) {
@@ -574,14 +580,12 @@ __global__ void kv_pack_v_kernel(const uint8_t* __restrict__ codes, int B, int L
       w[k] = code(2 * t, dim) | (code(2 * t + 1, dim) << 8) | (code(2 * t + 8, dim) << 16) |
              (code(2 * t + 9, dim) << 24);
     } else {
-      w[k] = 0;
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int dim = 8 * (8 * c + 2 * k + hb) + gr;
-        const uint32_t half = code(2 * t, dim) | (code(2 * t + 1, dim) << 4) | (code(2 * t + 8, dim) << 8) |
-                              (code(2 * t + 9, dim) << 12);
-        w[k] |= half << (16 * hb);
-      }
+      // word p = 4c + k: nibbles 0, 4 = tokens 2t, 2t+1 of dimension 16p + gr;
+      // 1, 5 = tokens 2t+8, 2t+9; 2, 6 and 3, 7 the same for dimension 16p + 8 + gr
+      const int p = 4 * c + k, da = 16 * p + gr, db = da + 8;
+      w[k] = code(2 * t, da) | (code(2 * t + 8, da) << 4) | (code(2 * t, db) << 8) | (code(2 * t + 8, db) << 12) |
+             (code(2 * t + 1, da) << 16) | (code(2 * t + 9, da) << 20) | (code(2 * t + 1, db) << 24) |
+             (code(2 * t + 9, db) << 28);
     }
   }
   reinterpret_cast<uint4*>(tiles)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
