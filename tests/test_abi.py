@@ -88,3 +88,48 @@ def test_library_has_sm103a_code():
     """The build targets sm_103a only (checked from the build flags)."""
     from w4a16_quantized_gemm_gb300 import build
     assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_new_entry_points_reject_bad_host_arguments(lib):
+    """Argument checks of the quantisers, the KV cache and W8A8 entry points run on
+    the host before any launch (fake device addresses: nothing is dereferenced)."""
+    a16, odd = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 1)
+    INVALID, ALIGN, UNSUP, OK = 1, 2, 3, 0
+    # RTN quantiser
+    assert lib.tm_quantize_rtn(None, 128, 16, 128, a16, a16, a16, None) == INVALID
+    assert lib.tm_quantize_rtn(a16, 100, 16, 128, a16, a16, a16, None) == INVALID     # K % g
+    assert lib.tm_quantize_rtn(odd, 128, 16, 128, a16, a16, a16, None) == ALIGN
+    # KV cache
+    assert lib.tm_kv_quantize(None, 4, 128, 8, a16, a16, a16, None) == INVALID
+    assert lib.tm_kv_quantize(a16, 4, 128, 5, a16, a16, a16, None) == INVALID         # bits
+    assert lib.tm_kv_quantize(a16, 4, 96, 8, a16, a16, a16, None) == INVALID          # D
+    assert lib.tm_kv_quantize(odd, 4, 128, 8, a16, a16, a16, None) == ALIGN
+    assert lib.tm_kv_pack_v(None, 1, 16, 8, 8, a16, None) == INVALID
+    assert lib.tm_kv_pack_v(a16, 1, 20, 8, 8, a16, None) == INVALID                   # L % 16
+    assert lib.tm_kv_pack_v(a16, 1, 16, 8, 8, odd, None) == ALIGN
+    attn = lambda *p, B=1, Hq=32, Hkv=8, L=16, D=128, bits=8, split=0, out=a16: lib.tm_kv_decode_attention(
+        *p, B, Hq, Hkv, L, D, bits, split, out, None)
+    assert attn(None, a16, a16, a16, a16, a16, a16, a16) == INVALID
+    assert attn(a16, a16, a16, a16, a16, a16, a16, a16, L=20) == INVALID              # L % 16
+    assert attn(a16, a16, a16, a16, a16, a16, a16, a16, D=64) == INVALID              # D
+    assert attn(a16, a16, a16, a16, a16, a16, a16, a16, Hq=48, Hkv=3) == UNSUP        # 16 heads per KV head
+    assert attn(a16, a16, a16, a16, a16, a16, a16, a16, split=3) == INVALID
+    assert attn(odd, a16, a16, a16, a16, a16, a16, a16) == ALIGN
+    assert attn(a16, a16, a16, a16, a16, a16, a16, a16, B=0) == OK                    # nothing to do
+    # W8A8
+    assert lib.tm_w8a8_quantize_act(None, 1, 128, a16, a16, None) == INVALID
+    assert lib.tm_w8a8_quantize_act(a16, 1, 100, a16, a16, None) == INVALID           # K % 16
+    assert lib.tm_w8a8_quantize_act(odd, 1, 128, a16, a16, None) == ALIGN
+    assert lib.tm_w8a8_quantize_act(a16, 0, 128, a16, a16, None) == OK                # no rows
+    h = ctypes.c_void_p()
+    assert lib.tm_w8_pack(None, a16, 128, 16, ctypes.byref(h)) == INVALID
+    assert lib.tm_w8_pack(a16, a16, 100, 16, ctypes.byref(h)) == INVALID              # K % 16
+    assert lib.tm_w8_pack(a16, a16, 128, 16, None) == INVALID
+    assert lib.tm_w8_unpack(None, a16, a16) == INVALID
+    assert lib.tm_w8_packed_info(None, None, None, None) == INVALID
+    lib.tm_w8_packed_free(None)
+    assert lib.tm_w8a8_gemm(None, a16, a16, a16, 1, 0, None) == INVALID
+    assert lib.tm_w8a8_gemm(a16, a16, a16, a16, 1, 3, None) == INVALID                 # split
+    assert lib.tm_w8a8_gemm_ex(a16, a16, a16, a16, 64, 0, 96, None) == INVALID         # tile_m
+    assert lib.tm_w8a8_gemm(odd, a16, a16, a16, 1, 0, None) == ALIGN
+    assert lib.tm_w8a8_gemm(a16, a16, a16, a16, 0, 0, None) == OK                      # M = 0

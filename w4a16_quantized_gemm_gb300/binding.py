@@ -324,7 +324,13 @@ def kv_decode_attention(Q: torch.Tensor, k: tuple, v: tuple, lengths: torch.Tens
     B, Hq, D = Q.shape
     kc, ks, kz = k
     vc, vs, vz = v
+    if kc.dim() != 4 or kc.shape[0] != B or tuple(lengths.shape) != (B,):
+        raise ValueError("key codes must be [B][Hkv][L][D*bits/8] and lengths [B], B as in Q")
+    if Q.dtype != torch.float16 or kc.dtype != torch.uint8 or vc.dtype != torch.uint8:
+        raise ValueError("Q must be fp16 and the codes uint8")
     Hkv, L = kc.shape[1], kc.shape[2]
+    if kc.shape[3] != D * bits // 8 or vc.numel() != B * Hkv * L * D * bits // 8:
+        raise ValueError("code sizes do not match D and bits")
     if tuple(ks.shape) != (B, Hkv, L) or tuple(vs.shape) != (B, Hkv, L):
         raise ValueError("scales and zeros must be [B][Hkv][L] like the key codes")
     if out is None:
