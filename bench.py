@@ -58,6 +58,25 @@ def flops(M, K, N):
     return 2 * M * N * K
 
 
+def rtn_bytes(K, N, g):
+    """RTN quantisation: read fp16 W; write one code and, per (group, column), one
+    zero byte and one fp16 scale."""
+    G = K // g
+    return 2 * K * N + K * N + G * N + 2 * G * N
+
+
+def kv_cache_bytes(B, L, Hkv, D, bits):
+    """K and V of B sequences of L tokens: codes plus an fp16 scale and a uint8
+    zero per (token, head)."""
+    return 2 * B * L * Hkv * (D * bits // 8 + 3)
+
+
+def w8a8_bytes(M, K, N):
+    """One W8A8 layer: the quantiser reads fp16 X and writes int8 X and s_x; the
+    GEMM reads the int8 weights, their fp32 scales, int8 X and s_x, writes fp16 Y."""
+    return (2 * M * K + M * K + 4 * M) + (K * N + 4 * N + M * K + 4 * M + 2 * M * N)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -521,7 +540,6 @@ def run_rtn(args, rank, world, local):
     import numpy as np
     import torch
 
-    import oracle.rtn as rtn_oracle
     from w4a16_quantized_gemm_gb300 import binding, synth
 
     torch.cuda.set_device(local)
@@ -537,7 +555,7 @@ def run_rtn(args, rank, world, local):
         z = torch.empty((K // g, N), dtype=torch.uint8, device=device)
         sc = torch.empty((K // g, N), dtype=torch.float16, device=device)
         layers.append({"name": name, "K": K, "N": N, "Wh": Wh, "W": W, "q": q, "z": z, "s": sc,
-                       "bytes": rtn_oracle.bytes_moved(K, N, g)})
+                       "bytes": rtn_bytes(K, N, g)})
     step_bytes = sum(L["bytes"] for L in layers)
     lib = binding.load()
     stream = torch.cuda.Stream(device)
@@ -605,6 +623,7 @@ def run_rtn(args, rank, world, local):
                "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt * 1e3 / steps, 3),
                "timing": "host wall clock; W copied in, quantised, codes/zeros/scales copied out"}
         if world == 1 and not args.no_cpu:
+            import oracle.rtn as rtn_oracle  # the CPU baseline leg only
             t0 = time.perf_counter()
             for L in layers:
                 rtn_oracle.quantize(L["Wh"], g)
@@ -730,7 +749,6 @@ def run_kv(args, rank, world, local):
     import numpy as np
     import torch
 
-    import oracle.kv as kv_oracle
     from w4a16_quantized_gemm_gb300 import binding, synth
 
     torch.cuda.set_device(local)
@@ -752,7 +770,7 @@ def run_kv(args, rank, world, local):
         caches.append((bits, binding.kv_quantize(K, bits), (binding.kv_pack_v(vq[0], bits), vq[1], vq[2]),
                        torch.empty((Bsz, Hq, D), dtype=torch.float16, device=device), vq[0]))
         del K, V
-    step_bytes = sum(kv_oracle.cache_bytes(Bsz, L, Hkv, D, bits) for bits in (8, 4)) + 2 * 2 * Bsz * Hq * D * 2
+    step_bytes = sum(kv_cache_bytes(Bsz, L, Hkv, D, bits) for bits in (8, 4)) + 2 * 2 * Bsz * Hq * D * 2
     stream = torch.cuda.Stream(device)
 
     def launch_all(st):
@@ -793,6 +811,7 @@ def run_kv(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu:
         # the fp64 oracle on the whole step (dequantise both caches, attention),
         # repeated for at least 10 s
+        import oracle.kv as kv_oracle  # the CPU baseline leg only
         host = [(bits, [t.cpu().numpy() for t in kq], [vcodes.cpu().numpy(), vq[1].cpu().numpy(), vq[2].cpu().numpy()])
                 for bits, kq, vq, _, vcodes in caches]
         q64 = Q.float().cpu().numpy().astype(np.float64)
@@ -840,7 +859,6 @@ def run_w8a8(args, rank, world, local, prefill=False):
     import numpy as np
     import torch
 
-    import oracle.w8a8 as w8_oracle
     from w4a16_quantized_gemm_gb300 import binding, synth
 
     torch.cuda.set_device(local)
@@ -852,11 +870,11 @@ def run_w8a8(args, rank, world, local, prefill=False):
     items = []
     for name in ("qkv", "o_proj", "gate_up", "down"):
         K, N = synth.LLAMA3_8B[name]
-        W = (synth.normal64(f"w8bench/W/{name}", K, N) * 0.02).astype(np.float16)
-        q, sw = w8_oracle.quantize_weight(W)
+        Wh = (synth.normal64(f"w8bench/W/{name}", K, N) * 0.02).astype(np.float16)
+        W = torch.from_numpy(Wh.view(np.uint16)).to(device).view(torch.float16)
+        qd, sd = binding.w8_quantize_weight(W)  # the per-channel quantiser on the GPU
         del W
-        host[name] = (q, sw)
-        qd, sd = torch.from_numpy(q).to(device), torch.from_numpy(sw).to(device)
+        host[name] = Wh
         for M in Ms:
             X = torch.from_numpy(synth.activations(M, K, tag=f"/w8/{name}/M{M}").view(np.uint16)).to(device)
             X = X.view(torch.float16)
@@ -864,7 +882,7 @@ def run_w8a8(args, rank, world, local, prefill=False):
                           "xq": torch.empty((M, K), dtype=torch.int8, device=device),
                           "sx": torch.empty((M,), dtype=torch.float32, device=device),
                           "Y": torch.empty((M, N), dtype=torch.float16, device=device),
-                          "bytes": 2 * M * K + M * K + 4 * M + w8_oracle.algorithmic_bytes(M, K, N),
+                          "bytes": w8a8_bytes(M, K, N),
                           "flops": 2 * M * K * N})
         del qd, sd
     step_bytes = sum(it["bytes"] for it in items)
@@ -918,10 +936,12 @@ def run_w8a8(args, rank, world, local, prefill=False):
     if rank == 0 and world == 1 and not args.no_cpu:
         # the oracle (binary32 quantiser, exact int64 product) on the first
         # `cols` output columns of every GEMM of the step, scaled by N / cols
+        import oracle.w8a8 as w8_oracle  # the CPU baseline leg only
         cols = 64 if prefill else 2048
         t_sample = t_full = 0.0
+        qw = {name: w8_oracle.quantize_weight(Wh) for name, Wh in host.items()}
         for it in items:
-            q, sw = host[it["name"]]
+            q, sw = qw[it["name"]]
             Xh = it["X"].cpu().numpy()
             ts = time.perf_counter()
             qx, sx = w8_oracle.quantize_act(Xh)

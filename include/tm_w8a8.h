@@ -44,6 +44,16 @@ typedef struct tm_w8_packed tm_w8_packed;
 tm_status tm_w8a8_quantize_act(const uint16_t* X, int M, int K, int8_t* xq, float* sx, void* stream);
 
 /*
+ * Per-output-channel quantisation of fp16 weights (the rule above, per column n
+ * over the K rows), producing the inputs of tm_w8_pack.
+ *   W : device fp16 bits [K][N] row-major, 16-byte aligned; N % 16 == 0
+ *   q : device int8 [K][N], 8-byte aligned;  sw: device fp32 [N], 4-byte aligned
+ * Asynchronous on `stream`: a memset of sw and three launches (column maxima
+ * through an integer atomic max, the codes, the scales); no allocation.
+ */
+tm_status tm_w8_quantize_weight(const uint16_t* W, int K, int N, int8_t* q, float* sw, void* stream);
+
+/*
  * Offline repack of per-channel quantised weights into the GEMM's order.
  *   q : device int8 [K][N] row-major (codes -127..127)
  *   sw: device fp32 [N]

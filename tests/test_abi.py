@@ -133,3 +133,6 @@ def test_new_entry_points_reject_bad_host_arguments(lib):
     assert lib.tm_w8a8_gemm_ex(a16, a16, a16, a16, 64, 0, 96, None) == INVALID         # tile_m
     assert lib.tm_w8a8_gemm(odd, a16, a16, a16, 1, 0, None) == ALIGN
     assert lib.tm_w8a8_gemm(a16, a16, a16, a16, 0, 0, None) == OK                      # M = 0
+    assert lib.tm_w8_quantize_weight(None, 128, 16, a16, a16, None) == INVALID
+    assert lib.tm_w8_quantize_weight(a16, 128, 20, a16, a16, None) == INVALID        # N % 16
+    assert lib.tm_w8_quantize_weight(odd, 128, 16, a16, a16, None) == ALIGN

@@ -154,3 +154,33 @@ def test_rejects_bad_arguments():
         binding.pack_w8(torch.zeros((1000, 512), dtype=torch.int8, device="cuda"),
                         torch.ones(512, dtype=torch.float32, device="cuda"))
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("K,N", [(1024, 512), (1040, 272), (4096, 16), (600, 4096)])
+def test_quantize_weight_bit_exact(K, N):
+    """The GPU per-channel weight quantiser equals the binary32 oracle bit for bit
+    (K slices of 512 rows combined by the integer atomic max; a zero column)."""
+    W = _fp16(f"w8/Wq/{K}/{N}", K, N, 0.05)
+    W[:, 1] = 0
+    W[3, 2] = np.float16(-7.5)          # a column whose maximum magnitude is negative
+    q, sw = binding.w8_quantize_weight(torch.from_numpy(W.view(np.uint16)).cuda().view(torch.float16))
+    torch.cuda.synchronize()
+    q0, s0 = w8.quantize_weight(W)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), s0.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q0)
+
+
+def test_gpu_quantisers_pack_gemm_pipeline():
+    """fp16 W and X through the GPU quantisers, the packer and the GEMM equal the
+    oracle pipeline."""
+    K, N, M = 2048, 1024, 7
+    W = _fp16("w8/pipeW", K, N, 0.05)
+    X = _acts(M, K, tag="pipeW")
+    q, sw = binding.w8_quantize_weight(torch.from_numpy(W.view(np.uint16)).cuda().view(torch.float16))
+    xq, sx = binding.w8a8_quantize_act(torch.from_numpy(X.view(np.uint16)).cuda().view(torch.float16))
+    Y = binding.w8a8_gemm(xq, sx, binding.pack_w8(q, sw))
+    torch.cuda.synchronize()
+    q0, s0 = w8.quantize_weight(W)
+    qx0, sx0 = w8.quantize_act(X)
+    ref = w8.gemm(qx0, sx0, q0, s0)
+    assert oracle.rel_max_err(Y.float().cpu().numpy().astype(np.float64), ref) <= TOL

@@ -23,7 +23,8 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
-           "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex")
+           "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
+           "tm_w8_quantize_weight")
 
 
 class TMError(RuntimeError):
@@ -105,6 +106,8 @@ def load(path: Optional[str] = None):
     lib.tm_w8_packed_free.argtypes = [vp]
     lib.tm_w8a8_gemm.restype = ci
     lib.tm_w8a8_gemm.argtypes = [vp, vp, vp, vp, ci, ci, vp]
+    lib.tm_w8_quantize_weight.restype = ci
+    lib.tm_w8_quantize_weight.argtypes = [vp, ci, ci, vp, vp, vp]
     lib.tm_w8a8_gemm_ex.restype = ci
     lib.tm_w8a8_gemm_ex.argtypes = [vp, vp, vp, vp, ci, ci, ci, vp]
     _lib = lib
@@ -382,6 +385,21 @@ def w8a8_quantize_act(X: torch.Tensor, out: Optional[tuple] = None, stream: Opti
                                        _dev(sx, torch.float32, "sx"), ctypes.c_void_p(st.cuda_stream)),
            "tm_w8a8_quantize_act")
     return xq, sx
+
+
+def w8_quantize_weight(W: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """Per-output-channel int8 quantisation of fp16 W [K][N] on the GPU (see
+    tm_w8_quantize_weight): returns (q int8 [K][N], sw fp32 [N]), the inputs of
+    ``pack_w8``."""
+    if W.dim() != 2 or W.dtype != torch.float16:
+        raise ValueError("W must be fp16 [K][N]")
+    K, N = W.shape
+    q = torch.empty((K, N), dtype=torch.int8, device=W.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device)
+    st = stream if stream is not None else torch.cuda.current_stream(W.device)
+    _check(load().tm_w8_quantize_weight(_dev(W, torch.float16, "W"), K, N, q.data_ptr(), sw.data_ptr(),
+                                        ctypes.c_void_p(st.cuda_stream)), "tm_w8_quantize_weight")
+    return q, sw
 
 
 class W8Packed:

@@ -110,6 +110,80 @@ __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restr
   }
 }
 
+// Per-channel weight quantisation, three launches after zeroing sw: the column
+// maxima of |w| (a block per 256 columns x a slice of K, combined with an
+// integer atomic max -- the patterns of non-negative floats order like the
+// floats), then the codes with s = max / 127 recomputed per block, then sw
+// itself in place.
+constexpr int kWqRows = 512;  // rows of K per block
+
+__global__ void __launch_bounds__(256) w8_colmax_kernel(const __half* __restrict__ W, int K, int N,
+                                                         uint32_t* __restrict__ amax) {
+  __shared__ float red[8][32][8];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c8 = blockIdx.x * 32 + tx, N8 = N / 8;
+  const int k0 = blockIdx.y * kWqRows, k1 = min(K, k0 + kWqRows);
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (c8 < N8) {
+    for (int k = k0 + ty; k < k1; k += 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(W + (size_t)k * N + 8 * c8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        a[2 * e] = fmaxf(a[2 * e], fabsf(f.x));
+        a[2 * e + 1] = fmaxf(a[2 * e + 1], fabsf(f.y));
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) red[ty][tx][c] = a[c];
+  __syncthreads();
+  if (ty == 0 && c8 < N8) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float m = red[0][tx][c];
+#pragma unroll
+      for (int y = 1; y < 8; ++y) m = fmaxf(m, red[y][tx][c]);
+      atomicMax(amax + 8 * c8 + c, __float_as_uint(m));
+    }
+  }
+}
+
+__device__ __forceinline__ float w8_scale_of(uint32_t amax_bits) {
+  const float a = __uint_as_float(amax_bits);
+  return a == 0.f ? 1.f : __fdiv_rn(a, 127.f);
+}
+
+__global__ void __launch_bounds__(256) w8_wquant_kernel(const __half* __restrict__ W, int K, int N,
+                                                         const uint32_t* __restrict__ amax, int8_t* __restrict__ q) {
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c8 = blockIdx.x * 32 + tx, N8 = N / 8;
+  if (c8 >= N8) return;
+  const int k0 = blockIdx.y * kWqRows, k1 = min(K, k0 + kWqRows);
+  float inv[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) inv[c] = __fdiv_rn(1.f, w8_scale_of(amax[8 * c8 + c]));
+  for (int k = k0 + ty; k < k1; k += 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(W + (size_t)k * N + 8 * c8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t b[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+      b[2 * e] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.x, inv[2 * e])), -127.f), 127.f) & 0xFFu;
+      b[2 * e + 1] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.y, inv[2 * e + 1])), -127.f), 127.f) & 0xFFu;
+    }
+    *reinterpret_cast<uint2*>(q + (size_t)k * N + 8 * c8) =
+        make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+  }
+}
+
+__global__ void w8_scale_kernel(float* __restrict__ sw, int N) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n < N) sw[n] = w8_scale_of(__float_as_uint(sw[n]));
+}
+
 // ------------------------------------------------------------- packing -----
 
 // One thread per 16-byte chunk of the packed codes: chunk c of row n of block
@@ -841,6 +915,25 @@ extern "C" tm_status tm_w8a8_quantize_act(const uint16_t* X, int M, int K, int8_
   if (cudaLaunchKernelEx(&cfg, w8_quant_act_kernel, reinterpret_cast<const __half*>(X), K, xq, sx) != cudaSuccess)
     return TM_ERR_CUDA;
   set_launch_count(1);
+  return TM_OK;
+}
+
+extern "C" tm_status tm_w8_quantize_weight(const uint16_t* W, int K, int N, int8_t* q, float* sw, void* stream) {
+  if (!W || !q || !sw || K <= 0 || N <= 0 || N % 16) return TM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(W) & 15u) || (reinterpret_cast<uintptr_t>(q) & 7u) ||
+      (reinterpret_cast<uintptr_t>(sw) & 3u))
+    return TM_ERR_ALIGNMENT;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid((unsigned)((N / 8 + 31) / 32), (unsigned)((K + kWqRows - 1) / kWqRows));
+  if (grid.y > 65535u) return TM_ERR_UNSUPPORTED;
+  auto* Wh = reinterpret_cast<const __half*>(W);
+  auto* amax = reinterpret_cast<uint32_t*>(sw);  // the maxima live in sw until the last launch
+  if (cudaMemsetAsync(sw, 0, (size_t)N * 4, st) != cudaSuccess) return TM_ERR_CUDA;
+  w8_colmax_kernel<<<grid, 256, 0, st>>>(Wh, K, N, amax);
+  w8_wquant_kernel<<<grid, 256, 0, st>>>(Wh, K, N, amax, q);
+  w8_scale_kernel<<<(unsigned)((N + 255) / 256), 256, 0, st>>>(sw, N);
+  if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
+  set_launch_count(3);
   return TM_OK;
 }
 
