@@ -310,6 +310,8 @@ def kv_quantize(X: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] 
 def kv_pack_v(codes: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Value codes [B][Hkv][L][D*bits/8] -> the 16-token tiles in MMA lane
     order the attention kernel reads (see tm_kv_pack_v)."""
+    if codes.dim() != 4 or codes.dtype != torch.uint8 or codes.shape[3] != 128 * bits // 8:
+        raise ValueError("codes must be uint8 [B][Hkv][L][128*bits/8]")
     B, Hkv, L, _ = codes.shape
     codes = codes.contiguous()
     tiles = torch.empty(B * Hkv * L * 128 * bits // 8, dtype=torch.uint8, device=codes.device)
@@ -454,6 +456,8 @@ def w8a8_gemm(xq: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[tor
     if xq.dim() != 2 or xq.shape[1] != w.K:
         raise ValueError("xq must be int8 [M][K]")
     M = xq.shape[0]
+    if tuple(sx.shape) != (M,):
+        raise ValueError("sx must be fp32 [M]")
     if out is None:
         out = torch.empty((M, w.N), dtype=torch.float16, device=xq.device)
     if tuple(out.shape) != (M, w.N):
