@@ -138,6 +138,23 @@ tm_status tm_kv_quantize(const uint16_t* X, long long rows, int D, int bits, uin
 tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, int bits, uint8_t* tiles, void* stream);
 
 /*
+ * Online append to the head-major cache: the new token of every (sequence b,
+ * KV head) is quantised by the rule of tm_kv_quantize and written at position
+ * pos[b] -- key codes, ks, kz, vs, vz in place and the value codes into the
+ * 16-token tile of tm_kv_pack_v's layout (int4: the byte shared with token
+ * pos +- 8 is read, modified and written).  Positions outside 0..L-1 are
+ * ignored.  One token per sequence per call.
+ *   Kn, Vn : device fp16 [B][Hkv][D], D = 128, 8-byte aligned
+ *   pos    : device int32 [B]
+ *   kc, ks, kz, vtiles, vs, vz: the cache of tm_kv_decode_attention (kc 4-byte,
+ *            ks and vs 2-byte aligned), L % 16 == 0
+ * Asynchronous on `stream`, one launch.
+ */
+tm_status tm_kv_append(const uint16_t* Kn, const uint16_t* Vn, const int* pos, int B, int Hkv, int L, int D, int bits,
+                       uint8_t* kc, uint16_t* ks, uint8_t* kz, uint8_t* vtiles, uint16_t* vs, uint8_t* vz,
+                       void* stream);
+
+/*
  * Decode attention over a quantised KV cache, one query token per sequence,
  * on tensor cores (mma.m16n8k16 on the codes as exact fp16 integers):
  *   out[b][h] = sum_t p_t v~_t,  p = softmax_t(q[b][h] . k~_t / sqrt(D)),

@@ -116,6 +116,13 @@ def test_new_entry_points_reject_bad_host_arguments(lib):
     assert attn(a16, a16, a16, a16, a16, a16, a16, a16, split=3) == INVALID
     assert attn(odd, a16, a16, a16, a16, a16, a16, a16) == ALIGN
     assert attn(a16, a16, a16, a16, a16, a16, a16, a16, B=0) == OK                    # nothing to do
+    app = lambda *p, B=1, Hkv=8, L=16, D=128, bits=8: lib.tm_kv_append(p[0], p[1], p[2], B, Hkv, L, D, bits,
+                                                                        *p[3:], None)
+    assert app(None, a16, a16, a16, a16, a16, a16, a16, a16) == INVALID
+    assert app(a16, a16, a16, a16, a16, a16, a16, a16, a16, L=20) == INVALID          # L % 16
+    assert app(a16, a16, a16, a16, a16, a16, a16, a16, a16, bits=6) == INVALID
+    assert app(odd, a16, a16, a16, a16, a16, a16, a16, a16) == ALIGN
+    assert app(a16, a16, a16, a16, a16, a16, a16, a16, a16, B=0) == OK
     # W8A8
     assert lib.tm_w8a8_quantize_act(None, 1, 128, a16, a16, None) == INVALID
     assert lib.tm_w8a8_quantize_act(a16, 1, 100, a16, a16, None) == INVALID           # K % 16

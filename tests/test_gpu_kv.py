@@ -161,3 +161,41 @@ def test_attention_rejects_misaligned_cache():
     with pytest.raises(binding.TMError) as e:
         binding.kv_decode_attention(Q, (c, s, z_off), (c, s, z), lens, 8)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_append_token_by_token_equals_bulk(bits):
+    """Appending the tokens one decode step at a time (tm_kv_append) builds the
+    same cache, bit for bit, as quantising them in bulk and packing the value
+    tiles; positions outside the cache are ignored."""
+    B, Hkv, L, D = 2, 8, 48, 128
+    K = _fp16(f"app/K/{bits}", B, Hkv, L, D)   # head-major
+    V = _fp16(f"app/V/{bits}", B, Hkv, L, D)
+    RB = D * bits // 8
+    kc = torch.zeros((B, Hkv, L, RB), dtype=torch.uint8, device="cuda")
+    ks = torch.zeros((B, Hkv, L), dtype=torch.float16, device="cuda")
+    kz = torch.zeros((B, Hkv, L), dtype=torch.uint8, device="cuda")
+    vt = torch.zeros(B * Hkv * L * RB, dtype=torch.uint8, device="cuda")
+    vs = torch.zeros((B, Hkv, L), dtype=torch.float16, device="cuda")
+    vz = torch.zeros((B, Hkv, L), dtype=torch.uint8, device="cuda")
+    Kd = _dev(K.view(np.uint16)).view(torch.float16)
+    Vd = _dev(V.view(np.uint16)).view(torch.float16)
+    for step in range(L):
+        pos = torch.tensor([step, L - 1 - step], dtype=torch.int32, device="cuda")  # sequence 1 fills backwards
+        rows = torch.tensor([step, L - 1 - step], device="cuda")
+        Kn = torch.stack([Kd[b, :, int(rows[b])] for b in range(B)]).contiguous()
+        Vn = torch.stack([Vd[b, :, int(rows[b])] for b in range(B)]).contiguous()
+        binding.kv_append(Kn, Vn, pos, (kc, ks, kz), (vt, vs, vz), bits)
+    bad = torch.tensor([-1, L], dtype=torch.int32, device="cuda")       # ignored
+    binding.kv_append(torch.ones_like(Kn), torch.ones_like(Vn), bad, (kc, ks, kz), (vt, vs, vz), bits)
+    torch.cuda.synchronize()
+    kq = binding.kv_quantize(Kd, bits)
+    vq = binding.kv_quantize(Vd, bits)
+    tiles = binding.kv_pack_v(vq[0], bits)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, kq[0]) and torch.equal(kz, kq[2]) and torch.equal(ks.view(torch.int16), kq[1].view(torch.int16))
+    assert torch.equal(vz, vq[2]) and torch.equal(vs.view(torch.int16), vq[1].view(torch.int16))
+    assert torch.equal(vt, tiles)
+    # and against the oracle's quantiser
+    c0, s0, z0 = kv.quantize(K, bits)
+    assert np.array_equal(kc.cpu().numpy(), c0) and np.array_equal(kz.cpu().numpy(), z0)

@@ -24,7 +24,7 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
            "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
-           "tm_w8_quantize_weight")
+           "tm_w8_quantize_weight", "tm_kv_append")
 
 
 class TMError(RuntimeError):
@@ -86,6 +86,8 @@ def load(path: Optional[str] = None):
     lib.tm_kv_quantize.argtypes = [vp, ctypes.c_longlong, ci, ci, vp, vp, vp, vp]
     lib.tm_kv_pack_v.restype = ci
     lib.tm_kv_pack_v.argtypes = [vp, ci, ci, ci, ci, vp, vp]
+    lib.tm_kv_append.restype = ci
+    lib.tm_kv_append.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci] + [vp] * 7
     lib.tm_kv_decode_attention.restype = ci
     lib.tm_kv_decode_attention.argtypes = [vp] * 8 + [ci] * 7 + [vp, vp]
     lib.tm_selftest_wait_timeout.restype = ci
@@ -319,6 +321,28 @@ def kv_pack_v(codes: torch.Tensor, bits: int, stream: Optional[torch.cuda.Stream
     _check(load().tm_kv_pack_v(codes.data_ptr(), B, L, Hkv, bits, tiles.data_ptr(), ctypes.c_void_p(st.cuda_stream)),
            "tm_kv_pack_v")
     return tiles
+
+
+def kv_append(Kn: torch.Tensor, Vn: torch.Tensor, pos: torch.Tensor, k: tuple, v: tuple, bits: int,
+              stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Quantise the new token's K and V (fp16 [B][Hkv][D]) into the head-major
+    cache at positions pos (int32 [B]); k = (codes, s, z), v = (tiles, s, z) as
+    for kv_decode_attention (see tm_kv_append)."""
+    kc, ks, kz = k
+    vc, vs, vz = v
+    B, Hkv, D = Kn.shape
+    if tuple(Vn.shape) != (B, Hkv, D) or kc.dim() != 4 or kc.shape[0] != B or kc.shape[1] != Hkv:
+        raise ValueError("Kn, Vn must be [B][Hkv][D] over a [B][Hkv][L][.] cache")
+    if pos.dtype != torch.int32 or tuple(pos.shape) != (B,):
+        raise ValueError("pos must be int32 [B]")
+    L = kc.shape[2]
+    ts = [Kn, Vn, pos, kc, ks, kz, vc, vs, vz]
+    if any((not t.is_cuda) or (not t.is_contiguous()) for t in ts):
+        raise ValueError("all tensors must be contiguous CUDA tensors")
+    st = stream if stream is not None else torch.cuda.current_stream(Kn.device)
+    _check(load().tm_kv_append(Kn.data_ptr(), Vn.data_ptr(), pos.data_ptr(), B, Hkv, L, D, bits, kc.data_ptr(),
+                               ks.data_ptr(), kz.data_ptr(), vc.data_ptr(), vs.data_ptr(), vz.data_ptr(),
+                               ctypes.c_void_p(st.cuda_stream)), "tm_kv_append")
 
 
 def kv_decode_attention(Q: torch.Tensor, k: tuple, v: tuple, lengths: torch.Tensor, bits: int, split: int = 0,

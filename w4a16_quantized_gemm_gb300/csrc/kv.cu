@@ -591,6 +591,84 @@ __global__ void kv_pack_v_kernel(const uint8_t* __restrict__ codes, int B, int L
   reinterpret_cast<uint4*>(tiles)[idx] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Online append: the new token of every (sequence, KV head) -- one warp each,
+// lane l holding dimensions 4l .. 4l+3 -- quantised by the rule above and
+// written at position pos[b] of the head-major cache: key codes, scales and
+// zeros in place, the value codes into their bytes (int8) or nibbles (int4,
+// read-modify-write of the byte shared with token pos +- 8) of the 16-token
+// tile.  One token per sequence per launch, so no two lanes touch one byte.
+template <int BITS>
+__global__ void __launch_bounds__(128) kv_append_kernel(const __half* __restrict__ Kn, const __half* __restrict__ Vn,
+                                                         const int* __restrict__ pos, int B, int Hkv, int L,
+                                                         uint8_t* __restrict__ kc, __half* __restrict__ ks,
+                                                         uint8_t* __restrict__ kz, uint8_t* __restrict__ vt,
+                                                         __half* __restrict__ vs, uint8_t* __restrict__ vz) {
+  constexpr int RB = kAttnD * BITS / 8;
+  const int bh = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (bh >= B * Hkv) return;
+  const int b = bh / Hkv;
+  const int p = pos[b];
+  if (p < 0 || p >= L) return;  // outside the cache: ignored
+  const size_t row = (size_t)bh * L + p;
+  constexpr float kB = (float)((1 << BITS) - 1);
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint2 raw = *reinterpret_cast<const uint2*>((which ? Vn : Kn) + (size_t)bh * kAttnD + 4 * lane);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+    const float v[4] = {f0.x, f0.y, f1.x, f1.y};
+    float lo = fminf(fminf(fminf(0.f, v[0]), fminf(v[1], v[2])), v[3]);
+    float hi = fmaxf(fmaxf(fmaxf(0.f, v[0]), fmaxf(v[1], v[2])), v[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    float r = hi - lo;
+    if (r == 0.f) r = kB;
+    __half sh = __float2half_rn(__fdiv_rn(r, kB));
+    const __half tiny = __ushort_as_half((unsigned short)1);  // 2^-24
+    if (__half2float(sh) < __half2float(tiny)) sh = tiny;
+    const float sf = __half2float(sh);
+    const float zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), kB);
+    const float inv = __fdiv_rn(1.f, sf);
+    uint32_t c[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) c[e] = (uint32_t)fminf(fmaxf(rintf(__fmul_rn(v[e], inv)) + zf, 0.f), kB);
+    if (which == 0) {
+      if constexpr (BITS == 8) {
+        *reinterpret_cast<uint32_t*>(kc + row * RB + 4 * lane) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+      } else {
+        *reinterpret_cast<uint16_t*>(kc + row * RB + 2 * lane) = (uint16_t)(c[0] | (c[1] << 4) | (c[2] << 8) | (c[3] << 12));
+      }
+      if (lane == 0) {
+        ks[row] = sh;
+        kz[row] = (uint8_t)zf;
+      }
+    } else {
+      uint8_t* tile = vt + ((size_t)bh * (L / 16) + p / 16) * (16 * RB);
+      const int tau = p & 15, t = (tau & 7) >> 1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 4 * lane + e;
+        if constexpr (BITS == 8) {
+          const int q8 = d >> 3, gr = d & 7;
+          tile[(q8 >> 2) * 512 + (4 * gr + t) * 16 + 4 * (q8 & 3) + (tau & 1) + 2 * (tau >> 3)] = (uint8_t)c[e];
+        } else {
+          const int pm = d >> 4, rr = d & 15, gr = rr & 7;
+          const int nib = (tau >> 3) + 2 * (rr >> 3) + 4 * (tau & 1);
+          uint8_t* byte = tile + (pm >> 2) * 512 + (4 * gr + t) * 16 + 4 * (pm & 3) + (nib >> 1);
+          *byte = (nib & 1) ? (uint8_t)((*byte & 0x0Fu) | (c[e] << 4)) : (uint8_t)((*byte & 0xF0u) | c[e]);
+        }
+      }
+      if (lane == 0) {
+        vs[row] = sh;
+        vz[row] = (uint8_t)zf;
+      }
+    }
+  }
+}
+
 template <int BITS, int G>
 tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
   constexpr uint32_t smem = KvSlot<BITS>::kSmem;
@@ -736,6 +814,32 @@ extern "C" tm_status tm_kv_pack_v(const uint8_t* codes, int B, int L, int Hkv, i
     kv_pack_v_kernel<8><<<grid, 256, 0, st>>>(codes, B, L, Hkv, tiles);
   } else {
     kv_pack_v_kernel<4><<<grid, 256, 0, st>>>(codes, B, L, Hkv, tiles);
+  }
+  if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
+  set_launch_count(1);
+  return TM_OK;
+}
+
+extern "C" tm_status tm_kv_append(const uint16_t* Kn, const uint16_t* Vn, const int* pos, int B, int Hkv, int L, int D,
+                                  int bits, uint8_t* kc, uint16_t* ks, uint8_t* kz, uint8_t* vtiles, uint16_t* vs,
+                                  uint8_t* vz, void* stream) {
+  if (!Kn || !Vn || !pos || !kc || !ks || !kz || !vtiles || !vs || !vz) return TM_ERR_INVALID_ARG;
+  if (B < 0 || Hkv <= 0 || L <= 0 || L % 16 != 0 || D != kAttnD || (bits != 4 && bits != 8))
+    return TM_ERR_INVALID_ARG;
+  if (((reinterpret_cast<uintptr_t>(Kn) | reinterpret_cast<uintptr_t>(Vn)) & 7u) ||
+      (reinterpret_cast<uintptr_t>(kc) & 3u) || ((reinterpret_cast<uintptr_t>(ks) | reinterpret_cast<uintptr_t>(vs)) & 1u))
+    return TM_ERR_ALIGNMENT;
+  if (B == 0) return TM_OK;
+  const unsigned grid = (unsigned)((B * Hkv + 3) / 4);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto* Kh = reinterpret_cast<const __half*>(Kn);
+  auto* Vh = reinterpret_cast<const __half*>(Vn);
+  if (bits == 8) {
+    kv_append_kernel<8><<<grid, 128, 0, st>>>(Kh, Vh, pos, B, Hkv, L, kc, reinterpret_cast<__half*>(ks), kz, vtiles,
+                                              reinterpret_cast<__half*>(vs), vz);
+  } else {
+    kv_append_kernel<4><<<grid, 128, 0, st>>>(Kh, Vh, pos, B, Hkv, L, kc, reinterpret_cast<__half*>(ks), kz, vtiles,
+                                              reinterpret_cast<__half*>(vs), vz);
   }
   if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
   set_launch_count(1);
