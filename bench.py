@@ -399,33 +399,31 @@ def per_gemm_detail(wl, stream, peaks, min_bytes=300e6, reps=5):
 
 
 def run_e2e(wl, args, spec):
-    """Public call with host buffers, one step at a time: every GEMM's X copied
-    in from pinned host memory, the step's products (tm_w4a16_gemm through the
-    binding), every Y copied back to pinned host memory, one synchronisation
-    per step; host wall clock."""
+    """Public call with host buffers, one step at a time: tm_w4a16_gemm_host_batch
+    (every GEMM's X in one copy from pinned host memory, the step's products in
+    order, every Y back in one copy to pinned host memory), one synchronisation
+    per step; host wall clock.  The first step's results are compared bit for
+    bit with the device-resident run's outputs."""
     import numpy as np
     import torch
 
     from w4a16_quantized_gemm_gb300 import binding
 
-    hostX = [torch.from_numpy(it["Xh"].view(np.uint16)).view(torch.float16).pin_memory() for it in wl.items]
-    hostY = [torch.empty(tuple(it["Y"].shape), dtype=torch.float16, pin_memory=True) for it in wl.items]
-    h2d = sum(x.numel() * 2 for x in hostX)
-    d2h = sum(y.numel() * 2 for y in hostY)
+    batch = binding.HostBatch([it["w"] for it in wl.items], [int(it["Xh"].shape[0]) for it in wl.items])
+    for i, it in enumerate(wl.items):
+        batch.x(i).copy_(torch.from_numpy(it["Xh"].view(np.uint16)).view(torch.float16))
+    h2d = batch.X_host.numel() * 2
+    d2h = batch.Y_host.numel() * 2
     stream = torch.cuda.Stream()
 
     def step():
-        with torch.cuda.stream(stream):
-            for it, x in zip(wl.items, hostX):
-                it["X"].copy_(x, non_blocking=True)
-            for it in wl.items:
-                binding.gemm(it["X"], it["w"], out=it["Y"], stream=stream)
-            for it, y in zip(wl.items, hostY):
-                y.copy_(it["Y"], non_blocking=True)
-        stream.synchronize()
+        batch.run(stream)  # waits for the stream
 
+    step()
+    same = all(torch.equal(batch.y(i).view(torch.int16), it["Y"].cpu().view(torch.int16))
+               for i, it in enumerate(wl.items))
     steps = max(3, min(args.steps, 200))
-    for _ in range(3):
+    for _ in range(2):
         step()
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -434,8 +432,10 @@ def run_e2e(wl, args, spec):
     units = (wl.step_bytes / 1e9) if spec["unit"] == "GB/s" else (wl.step_flops / 1e12)
     return {"value": round(units * steps / dt, 2), "unit": spec["unit"], "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt * 1e3 / steps, 3),
-            "timing": "host wall clock; per step: every X copied in from pinned memory, the GEMMs, every Y "
-                      "copied out to pinned memory, one stream synchronisation"}
+            "bitwise_equal_to_device_run": same,
+            "timing": "host wall clock; per step one tm_w4a16_gemm_host_batch call: every X in one copy from "
+                      "pinned host memory, the GEMMs, every Y out in one copy to pinned host memory, one "
+                      "stream synchronisation"}
 
 
 # ------------------------------------------------------------ CPU baseline ---

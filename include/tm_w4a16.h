@@ -214,6 +214,40 @@ tm_status tm_w4a16_gemm_silu_mul(const void* X, const tm_packed* p, void* H, int
 tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config* cfg,
                            void* stream);
 
+/*
+ * The product with X and Y in host memory, all asynchronous on `stream`:
+ * X_host is copied into X_dev, the product (as tm_w4a16_gemm_ex) runs from
+ * X_dev into Y_dev, and Y_dev is copied back into Y_host.  The caller
+ * synchronises the stream before reading Y_host.
+ *   X_host: fp16 [M][K] row-major; Y_host: fp16 [M][N] row-major.  Pinned
+ *           (page-locked) host memory lets the copies run asynchronously;
+ *           pageable memory is accepted, the copies then block the caller.
+ *   X_dev, Y_dev: device buffers of at least M K and M N fp16, 16-byte aligned
+ *           (owned by the caller, so that the call allocates nothing).
+ * Arguments are checked and the launch planned before any copy is issued:
+ * TM_ERR_INVALID_ARG / TM_ERR_ALIGNMENT / TM_ERR_UNSUPPORTED leave every
+ * buffer untouched; TM_ERR_CUDA when a copy or the launch fails.
+ */
+tm_status tm_w4a16_gemm_host(const void* X_host, const tm_packed* p, void* Y_host, int M, void* X_dev, void* Y_dev,
+                             const tm_gemm_config* cfg, void* stream);
+
+/*
+ * n products with host inputs and outputs, staged through one copy each way
+ * (the form of a decode step: every layer's activations in, every result out):
+ *   X_host holds X_0 .. X_{n-1} back to back, X_i fp16 [M[i]][K_i] row-major
+ *   (K_i, N_i: the shape of p[i]); Y_host receives Y_0 .. Y_{n-1} the same way.
+ *   X_dev, Y_dev: device staging buffers of at least sum M[i] K_i and
+ *   sum M[i] N_i fp16, 16-byte aligned; every X_i and Y_i then starts on a
+ *   32-byte boundary (K_i % 64 == 0, N_i % 16 == 0).
+ * On `stream`: one host-to-device copy, the n products in order (automatic
+ * plans, as tm_w4a16_gemm), one device-to-host copy; asynchronous, the caller
+ * synchronises before reading Y_host.  Every product is planned before the
+ * first copy: a rejected argument leaves all buffers untouched.  M[i] == 0
+ * skips product i.  tm_last_launch_count reports the kernels of all n.
+ */
+tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, const int* M, const void* X_host, void* Y_host,
+                                   void* X_dev, void* Y_dev, void* stream);
+
 /* The settings tm_w4a16_gemm would use for this handle and M (all fields filled in). */
 tm_status tm_gemm_plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out);
 

@@ -143,3 +143,20 @@ def test_new_entry_points_reject_bad_host_arguments(lib):
     assert lib.tm_w8_quantize_weight(None, 128, 16, a16, a16, None) == INVALID
     assert lib.tm_w8_quantize_weight(a16, 128, 20, a16, a16, None) == INVALID        # N % 16
     assert lib.tm_w8_quantize_weight(odd, 128, 16, a16, a16, None) == ALIGN
+
+
+def test_host_buffer_entry_points_reject_bad_arguments(lib):
+    """tm_w4a16_gemm_host / tm_w4a16_gemm_host_batch check their arguments on the
+    host before any copy (fake device addresses: nothing is dereferenced)."""
+    a16, odd = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 1)
+    INVALID, OK = 1, 0
+    assert lib.tm_w4a16_gemm_host(a16, None, a16, 1, a16, a16, None, None) == INVALID   # no weights
+    assert lib.tm_w4a16_gemm_host(a16, None, a16, -1, a16, a16, None, None) == INVALID
+    assert lib.tm_w4a16_gemm_host(None, None, None, 0, None, None, None, None) == INVALID
+    assert lib.tm_w4a16_gemm_host_batch(-1, None, None, a16, a16, a16, a16, None) == INVALID
+    assert lib.tm_w4a16_gemm_host_batch(0, None, None, None, None, None, None, None) == OK   # nothing to do
+    assert lib.tm_w4a16_gemm_host_batch(2, None, None, a16, a16, a16, a16, None) == INVALID
+    ps = (ctypes.c_void_p * 2)(None, None)
+    ms = (ctypes.c_int * 2)(1, 1)
+    assert lib.tm_w4a16_gemm_host_batch(2, ps, ms, a16, a16, a16, odd, None) == INVALID    # null handle
+    assert lib.tm_last_launch_count() == 0

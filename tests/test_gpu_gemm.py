@@ -169,6 +169,68 @@ def test_host_buffers_end_to_end():
     assert err <= TOL
 
 
+def test_gemm_host_entry_point_with_staging_buffers():
+    """tm_w4a16_gemm_host with caller-owned device staging buffers, asynchronous
+    until the stream is synchronised; every element against the oracle."""
+    M, K, N, g = 37, 2048, 1040, 64
+    X = activations(M, K, N, g)
+    Xh = torch.from_numpy(X.view(np.uint16)).view(torch.float16).pin_memory()
+    Yh = torch.full((M, N), float("nan"), dtype=torch.float16).pin_memory()
+    Xd = torch.empty(M * K + 64, dtype=torch.float16, device="cuda")
+    Yd = torch.empty(M * N + 64, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    binding.gemm_host(Xh, packed(K, N, g), out=Yh, stream=s, X_dev=Xd, Y_dev=Yd, sync=False)
+    assert binding.last_launch_count() == 1
+    s.synchronize()
+    q, z, s_, _ = host_weights(K, N, g)
+    import oracle
+    err = oracle.rel_max_err(Yh.float().numpy().astype(np.float64), oracle.gemm(X, q, z, s_, g))
+    assert err <= TOL
+    # the staged copy of X is X itself, bit for bit
+    assert torch.equal(Xd[:M * K].cpu().view(torch.int16), Xh.view(-1).view(torch.int16))
+
+
+def test_gemm_host_rejects_before_copying():
+    w = packed(1024, 384, 128)
+    Xh = torch.ones((4, 1024), dtype=torch.float16).pin_memory()
+    Yh = torch.zeros((4, 384), dtype=torch.float16).pin_memory()
+    Xd = torch.zeros(4 * 1024 + 8, dtype=torch.float16, device="cuda")
+    Yd = torch.zeros(4 * 384 + 8, dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.TMError) as e:
+        binding.gemm_host(Xh, w, out=Yh, X_dev=Xd[1:], Y_dev=Yd)           # misaligned staging buffer
+    assert e.value.status == 2
+    with pytest.raises(binding.TMError) as e:
+        binding.gemm_host(Xh, w, out=Yh, X_dev=Xd, Y_dev=Yd, config={"path": 7})
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert float(Xd.abs().sum()) == 0.0 and float(Yh.abs().sum()) == 0.0
+
+
+def test_gemm_host_batch_matches_oracle_every_product():
+    """tm_w4a16_gemm_host_batch: one copy in, the products in order (decode and
+    tensor-memory paths mixed, one M = 0), one copy out."""
+    import oracle
+    shapes = [(5, 1024, 384, 128), (0, 512, 256, 64), (64, 2048, 1040, 64), (1, 4096, 4096, 128),
+              (33, 512, 2048, 128)]
+    ws = [packed(K, N, g, seed=i) for i, (M, K, N, g) in enumerate(shapes)]
+    batch = binding.HostBatch(ws, [sh[0] for sh in shapes])
+    Xs = []
+    for i, (M, K, N, g) in enumerate(shapes):
+        X = activations(M, K, N, g, seed=i)
+        Xs.append(X)
+        batch.x(i).copy_(torch.from_numpy(X.view(np.uint16)).view(torch.float16))
+    batch.Y_host.fill_(float("nan"))
+    batch.run()
+    assert binding.last_launch_count() == 4
+    for i, (M, K, N, g) in enumerate(shapes):
+        if M == 0:
+            continue
+        q, z, s, _ = host_weights(K, N, g, seed=i)
+        err = oracle.rel_max_err(batch.y(i).float().numpy().astype(np.float64), oracle.gemm(Xs[i], q, z, s, g))
+        assert err <= TOL, (i, err)
+    assert binding.device_error(clear=True) == 0
+
+
 def test_one_launch_per_call():
     w = packed(1024, 384, 128)
     X = torch.zeros((4, 1024), dtype=torch.float16, device="cuda")

@@ -69,3 +69,9 @@ def test_silu_mul_prefill_path_unsupported():
     with pytest.raises(binding.TMError) as e:
         binding.gemm_silu_mul(X, w, config={"path": 2})
     assert e.value.status == 3
+
+
+def test_silu_mul_tc_multi_wave_tiles():
+    # more output tiles than SMs: the later waves carry the fused epilogue too
+    # (the sampled rows include the ragged last row tile)
+    _check(1500, 256, 8192, 128, {"path": 3, "split_k": 1, "tile_m": 128})

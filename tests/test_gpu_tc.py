@@ -100,3 +100,31 @@ def test_tc_one_launch_and_no_device_errors():
     assert binding.last_launch_count() == 1
     torch.cuda.synchronize()
     assert binding.device_error(clear=False) == 0
+
+
+# More output tiles (128 columns x tile_m rows) than a GB300 has SMs (152),
+# so that later waves of CTAs (one per SM: each holds all of tensor memory)
+# reuse the SMs, with a ragged last row tile and a ragged last column tile;
+# every row compared.
+@pytest.mark.parametrize("M,K,N,g,tile_m", [(2049, 256, 4112, 128, 256), (1100, 128, 2320, 64, 64),
+                                             (333, 64, 8208, 64, 16)])
+def test_tc_multi_wave_tiles_every_row(M, K, N, g, tile_m):
+    cfg = {"path": 3, "split_k": 1, "tile_m": tile_m}
+    tiles = -(-N // 128) * -(-M // tile_m)
+    assert tiles > 152
+    err, _ = run_and_compare(M, K, N, g, config=cfg, rows=list(range(M)))
+    assert err <= TOL, err
+
+
+def test_tc_split_and_unsplit_launches_agree():
+    # the same product without a K split (several waves) and with a split of 2
+    # (clusters reducing through distributed shared memory) agrees to the
+    # parity bar on every element
+    M, K, N, g = 700, 512, 6144, 128
+    w = packed(K, N, g)
+    X = torch.from_numpy(activations(M, K, N, g).view(np.uint16)).cuda().view(torch.float16)
+    Y1 = binding.gemm(X, w, config={"path": 3, "split_k": 1, "tile_m": 128}).float()
+    Y2 = binding.gemm(X, w, config={"path": 3, "split_k": 2, "tile_m": 128}).float()
+    torch.cuda.synchronize()
+    assert binding.device_error(clear=True) == 0
+    assert ((Y1 - Y2).abs().max() / Y2.abs().max()).item() <= TOL

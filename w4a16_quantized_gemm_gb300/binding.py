@@ -24,7 +24,7 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
            "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
-           "tm_w8_quantize_weight", "tm_kv_append")
+           "tm_w8_quantize_weight", "tm_kv_append", "tm_w4a16_gemm_host", "tm_w4a16_gemm_host_batch")
 
 
 class TMError(RuntimeError):
@@ -76,6 +76,10 @@ def load(path: Optional[str] = None):
     lib.tm_w4a16_gemm.argtypes = [vp, vp, vp, ci, vp]
     lib.tm_w4a16_gemm_ex.restype = ci
     lib.tm_w4a16_gemm_ex.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
+    lib.tm_w4a16_gemm_host.restype = ci
+    lib.tm_w4a16_gemm_host.argtypes = [vp, vp, vp, ci, vp, vp, ctypes.POINTER(GemmConfig), vp]
+    lib.tm_w4a16_gemm_host_batch.restype = ci
+    lib.tm_w4a16_gemm_host_batch.argtypes = [ci, ctypes.POINTER(vp), ctypes.POINTER(ci), vp, vp, vp, vp, vp]
     lib.tm_gemm_plan.restype = ci
     lib.tm_gemm_plan.argtypes = [vp, ci, ctypes.POINTER(GemmConfig), ctypes.POINTER(GemmConfig)]
     lib.tm_device_error.restype = ci
@@ -261,15 +265,86 @@ def gemm_silu_mul(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor]
 
 
 def _gemm_host(X, w, out, config, stream):
+    return gemm_host(X, w, out, config, stream)
+
+
+def _host_fp16(t: torch.Tensor, shape, name: str):
+    if t.is_cuda or t.dtype != torch.float16 or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host fp16 tensor of shape {tuple(shape)}")
+
+
+def _staging(t: Optional[torch.Tensor], numel: int, device, name: str) -> torch.Tensor:
+    if t is None:
+        return torch.empty(numel, dtype=torch.float16, device=device)
+    if not t.is_cuda or t.dtype != torch.float16 or not t.is_contiguous() or t.numel() < numel:
+        raise ValueError(f"{name} must be a contiguous CUDA fp16 buffer of at least {numel} elements")
+    return t
+
+
+def gemm_host(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = None, config=None,
+              stream: Optional[torch.cuda.Stream] = None, X_dev: Optional[torch.Tensor] = None,
+              Y_dev: Optional[torch.Tensor] = None, sync: bool = True) -> torch.Tensor:
+    """tm_w4a16_gemm_host: X fp16 [M][K] in host memory (pinned for speed) is
+    copied to the device buffer ``X_dev``, the product runs into ``Y_dev``, and
+    the result comes back into ``out`` (host fp16 [M][N]; pinned, allocated
+    when None).  Staging buffers are allocated when None.  With ``sync`` the
+    call waits for the stream; otherwise read ``out`` after synchronising it."""
+    if X.dim() != 2:
+        raise ValueError("X must be fp16 [M][K]")
+    M = X.shape[0]
+    _host_fp16(X, (M, w.K), "X")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float16, pin_memory=True)
+    _host_fp16(out, (M, w.N), "out")
+    X_dev = _staging(X_dev, M * w.K, w.device, "X_dev")
+    Y_dev = _staging(Y_dev, M * w.N, w.device, "Y_dev")
     s = stream if stream is not None else torch.cuda.current_stream(w.device)
-    with torch.cuda.stream(s):
-        Xd = X.to(w.device, non_blocking=True)
-        Yd = gemm(Xd, w, None, config, s)
-        if out is None:
-            out = torch.empty(Yd.shape, dtype=torch.float16, pin_memory=True)
-        out.copy_(Yd, non_blocking=True)
-    s.synchronize()
+    c = _cfg(config)
+    _check(load().tm_w4a16_gemm_host(X.data_ptr(), w.handle, out.data_ptr(), M, X_dev.data_ptr(), Y_dev.data_ptr(),
+                                     ctypes.byref(c) if c else None, ctypes.c_void_p(s.cuda_stream)),
+           "tm_w4a16_gemm_host")
+    if sync:
+        s.synchronize()
     return out
+
+
+class HostBatch:
+    """A fixed list of products with host inputs and outputs for
+    tm_w4a16_gemm_host_batch: ``X_host`` / ``Y_host`` are pinned buffers that
+    hold every X_i / Y_i back to back (``x(i)`` and ``y(i)`` are views of
+    them), staged through one device buffer each way."""
+
+    def __init__(self, weights, Ms, device=None):
+        if len(weights) != len(Ms) or any(m < 0 for m in Ms):
+            raise ValueError("one non-negative M per weight")
+        self.weights, self.Ms = list(weights), [int(m) for m in Ms]
+        dev = device if device is not None else (self.weights[0].device if self.weights else 0)
+        self.x_off, self.y_off = [0], [0]
+        for w, m in zip(self.weights, self.Ms):
+            self.x_off.append(self.x_off[-1] + m * w.K)
+            self.y_off.append(self.y_off[-1] + m * w.N)
+        self.X_host = torch.empty(self.x_off[-1], dtype=torch.float16, pin_memory=True)
+        self.Y_host = torch.empty(self.y_off[-1], dtype=torch.float16, pin_memory=True)
+        self.X_dev = torch.empty(self.x_off[-1], dtype=torch.float16, device=dev)
+        self.Y_dev = torch.empty(self.y_off[-1], dtype=torch.float16, device=dev)
+        n = len(self.weights)
+        self._p = (ctypes.c_void_p * max(1, n))(*[w.handle for w in self.weights])
+        self._m = (ctypes.c_int * max(1, n))(*self.Ms)
+
+    def x(self, i: int) -> torch.Tensor:
+        return self.X_host[self.x_off[i]:self.x_off[i + 1]].view(self.Ms[i], self.weights[i].K)
+
+    def y(self, i: int) -> torch.Tensor:
+        return self.Y_host[self.y_off[i]:self.y_off[i + 1]].view(self.Ms[i], self.weights[i].N)
+
+    def run(self, stream: Optional[torch.cuda.Stream] = None, sync: bool = True):
+        s = stream if stream is not None else torch.cuda.current_stream(self.X_dev.device)
+        _check(load().tm_w4a16_gemm_host_batch(len(self.weights), self._p, self._m, self.X_host.data_ptr(),
+                                               self.Y_host.data_ptr(), self.X_dev.data_ptr(),
+                                               self.Y_dev.data_ptr(), ctypes.c_void_p(s.cuda_stream)),
+               "tm_w4a16_gemm_host_batch")
+        if sync:
+            s.synchronize()
 
 
 def quantize_rtn(W: torch.Tensor, g: int, stream: Optional[torch.cuda.Stream] = None):

@@ -169,6 +169,59 @@ extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, i
   return tm_w4a16_gemm_ex(X, p, Y, M, nullptr, stream);
 }
 
+extern "C" tm_status tm_w4a16_gemm_host(const void* X_host, const tm_packed* p, void* Y_host, int M, void* X_dev,
+                                        void* Y_dev, const tm_gemm_config* cfg, void* stream) {
+  t_launches = 0;
+  if (!p || M < 0) return TM_ERR_INVALID_ARG;
+  if (M == 0) return TM_OK;
+  if (!X_host || !Y_host || !X_dev || !Y_dev) return TM_ERR_INVALID_ARG;
+  if (!aligned16(X_dev) || !aligned16(Y_dev)) return TM_ERR_ALIGNMENT;
+  tm_gemm_config c;
+  tm_status st = plan(p, M, cfg, &c);  // reject before touching any buffer
+  if (st != TM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)M * p->L.K * 2, yb = (size_t)M * p->L.N * 2;
+  if (cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return TM_ERR_CUDA;
+  st = tm_w4a16_gemm_ex(X_dev, p, Y_dev, M, &c, s);
+  if (st != TM_OK) return st;
+  return cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, s) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+}
+
+extern "C" tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, const int* M, const void* X_host,
+                                              void* Y_host, void* X_dev, void* Y_dev, void* stream) {
+  t_launches = 0;
+  if (n < 0 || (n > 0 && (!p || !M))) return TM_ERR_INVALID_ARG;
+  size_t xb = 0, yb = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!p[i] || M[i] < 0) return TM_ERR_INVALID_ARG;
+    if (M[i] == 0) continue;
+    tm_gemm_config c;
+    const tm_status st = plan(p[i], M[i], nullptr, &c);  // reject before touching any buffer
+    if (st != TM_OK) return st;
+    xb += (size_t)M[i] * p[i]->L.K * 2;
+    yb += (size_t)M[i] * p[i]->L.N * 2;
+  }
+  if (xb == 0) return TM_OK;
+  if (!X_host || !Y_host || !X_dev || !Y_dev) return TM_ERR_INVALID_ARG;
+  if (!aligned16(X_dev) || !aligned16(Y_dev)) return TM_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return TM_ERR_CUDA;
+  size_t xo = 0, yo = 0;
+  int launches = 0;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] == 0) continue;
+    const tm_status st = tm_w4a16_gemm_ex(static_cast<const char*>(X_dev) + xo, p[i],
+                                          static_cast<char*>(Y_dev) + yo, M[i], nullptr, stream);
+    if (st != TM_OK) return st;
+    launches += t_launches;
+    xo += (size_t)M[i] * p[i]->L.K * 2;
+    yo += (size_t)M[i] * p[i]->L.N * 2;
+  }
+  if (cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return TM_ERR_CUDA;
+  t_launches = launches;
+  return TM_OK;
+}
+
 extern "C" tm_status tm_device_error(int clear, uint32_t* bits) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TM_ERR_CUDA;
   uint32_t a = 0, b = 0, c = 0, d = 0, e = 0, f = 0, h = 0;
