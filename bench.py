@@ -640,7 +640,7 @@ def run_rtn(args, rank, world, local):
                    "l2": "inputs larger than L2 (698 MB of fp16 weights per step)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": peaks["source"], "kernel": "rtn_reg_kernel"},
+                     "peak_source": peaks["source"], "kernel": "rtn_tma_kernel"},
         "gpu_launches": len(layers) * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
     }
     if rank == 0:

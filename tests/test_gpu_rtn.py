@@ -26,6 +26,7 @@ def _gpu_quantize(W16, g):
 
 def _assert_bit_exact(W16, g):
     q, z, s = _gpu_quantize(W16, g)
+    assert binding.device_error(clear=True) == 0
     q0, z0, s0 = rtn.quantize(W16, g)
     assert np.array_equal(s, s0.view(np.uint16))
     assert np.array_equal(z, z0)
@@ -48,6 +49,17 @@ def test_rtn_special_values_bit_exact():
     W = np.stack(cols + cols, axis=1)  # 16 columns
     _assert_bit_exact(np.ascontiguousarray(W), 16)
     _assert_bit_exact(np.ascontiguousarray(W), 8)
+    # the same columns through the tiled kernel of g = 64 and g = 128 (tiles
+    # of 128 columns: these 16 are a ragged, zero-filled tile)
+    _assert_bit_exact(np.ascontiguousarray(np.tile(W, (4, 1))), 64)
+    _assert_bit_exact(np.ascontiguousarray(np.tile(W, (8, 1))), 128)
+
+
+@pytest.mark.parametrize("K,N,g", [(8192, 4112, 64), (2048, 2064, 128), (128, 144, 128)])
+def test_rtn_tiled_ragged_columns_bit_exact(K, N, g):
+    # N not a multiple of the 128-column tile; the first shape has more tiles
+    # (33 x 128) than two CTAs per SM take at once, so CTAs walk several
+    _assert_bit_exact(synth.fp16_weights(K, N, g), g)
 
 
 def test_rtn_quantize_pack_gemm_pipeline():

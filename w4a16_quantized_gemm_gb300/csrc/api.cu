@@ -87,6 +87,7 @@ static tm_status plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_g
 // Sticky error bits of the KV-cache kernels (kv.cu) and the W8A8 GEMM (w8a8.cu).
 cudaError_t kv_error_bits(uint32_t* bits, bool clear);
 cudaError_t w8_error_bits(uint32_t* bits, bool clear);
+cudaError_t rtn_error_bits(uint32_t* bits, bool clear);
 
 // Self-test of the bounded barrier wait every kernel uses: one warp waits on
 // an mbarrier that nothing ever arrives on; after kWaitLimitNs it must give
@@ -224,17 +225,18 @@ extern "C" tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, 
 
 extern "C" tm_status tm_device_error(int clear, uint32_t* bits) {
   if (cudaDeviceSynchronize() != cudaSuccess) return TM_ERR_CUDA;
-  uint32_t a = 0, b = 0, c = 0, d = 0, e = 0, f = 0, h = 0;
+  uint32_t a = 0, b = 0, c = 0, d = 0, e = 0, f = 0, h = 0, r = 0;
   if (pack_error_bits(&a, clear != 0) != cudaSuccess || decode_error_bits(&b, clear != 0) != cudaSuccess ||
       prefill_error_bits(&c, clear != 0) != cudaSuccess || tc_error_bits(&d, clear != 0) != cudaSuccess ||
       kv_error_bits(&f, clear != 0) != cudaSuccess || w8_error_bits(&h, clear != 0) != cudaSuccess ||
+      rtn_error_bits(&r, clear != 0) != cudaSuccess ||
       cudaMemcpyFromSymbol(&e, s_err_selftest, sizeof(e)) != cudaSuccess)
     return TM_ERR_CUDA;
   if (clear && e) {
     const uint32_t zero = 0;
     if (cudaMemcpyToSymbol(s_err_selftest, &zero, sizeof(zero)) != cudaSuccess) return TM_ERR_CUDA;
   }
-  const uint32_t v = (a | b | c | d | e | f | h) & kErrTimeout;
+  const uint32_t v = (a | b | c | d | e | f | h | r) & kErrTimeout;
   if (bits) *bits = v;
   return v ? TM_ERR_DEVICE_TIMEOUT : TM_OK;
 }

@@ -11,14 +11,20 @@
 // do not depend on how the work is split (one reciprocal per group and column
 // keeps the per-weight work at a multiply).
 //
-// HBM-bound: 2 bytes read and 1 byte written per weight.  A block owns 256
-// adjacent columns of one group: lane x of warp y holds 8 columns (16-byte
-// loads, 8-byte code stores; a warp moves 512 contiguous bytes per row) and
-// rows y, y + W, y + 2W, ... of the group (W warps), whose minima and maxima
-// the warps combine through shared memory.  For g = 64 and 128 (rtn_reg_kernel,
-// 8 warps) a thread keeps its g/8 rows in registers between the two passes,
-// so every weight is read from HBM once; other group sizes (rtn_kernel, 4
-// warps) read the group a second time, from L2.
+// HBM-bound: 2 bytes read and 1 byte written per weight.
+// g = 64 and 128 (rtn_tma_kernel): a persistent grid, two CTAs per SM, walks
+// tiles of one group's g rows x 128 columns.  One thread streams the tiles
+// with 2-D TMA copies into a ring of shared-memory slots; eight warps take a
+// tile each, warp w rows w g/8 .. (w + 1) g/8 - 1, lane l columns 4l .. 4l+3,
+// loading their rows into registers and releasing the slot at once; the
+// warps' column minima and maxima meet in shared memory (double-buffered
+// by tile parity, behind an mbarrier), and each thread writes its codes as
+// 4-byte stores (a warp writes 128 contiguous bytes per row).  Every weight
+// is read from HBM once and the ring keeps copies in flight while the warps
+// compute.  Other group sizes (rtn_kernel, 4 warps, 256 columns per block)
+// read the group a second time, from L2.
+#include <algorithm>
+
 #include "tm_common.cuh"
 
 namespace w4 {
@@ -136,68 +142,241 @@ __global__ void __launch_bounds__(kQuantThreads) rtn_kernel(const uint4* __restr
   }
 }
 
-constexpr int kRegThreads = 256;
-constexpr int kRegSlices = kRegThreads / kColGroups;  // 8 row slices
+static __device__ uint32_t s_err_rtn;
+
+constexpr int kTmaCols = 128;                      // columns per tile
+constexpr int kTmaWarps = 8;                       // quantising warps
+constexpr int kTmaThreads = 32 * (kTmaWarps + 1);  // + one producer warp
+constexpr int kTmaStages = 3;                      // ring slots
 
 template <int G>
-__global__ void __launch_bounds__(kRegThreads, 2) rtn_reg_kernel(const uint4* __restrict__ W, int N,
-                                                               uint2* __restrict__ q, uint2* __restrict__ z,
-                                                               uint4* __restrict__ s) {
-  constexpr int R = G / kRegSlices;  // rows per thread
-  __shared__ float s_lo[kRegSlices][kColGroups][kCols];
-  __shared__ float s_hi[kRegSlices][kColGroups][kCols];
-  const int tx = threadIdx.x % kColGroups, ty = threadIdx.x / kColGroups;
-  const int c8 = blockIdx.x * kColGroups + tx;
-  const int N8 = N / kCols;
-  const bool active = c8 < N8;
-  const int grp = blockIdx.y;
-  const uint4* w = W + (size_t)grp * G * N8 + c8;
-  uint4 v[R];
-  float lo[kCols], hi[kCols];
+struct RtnTmaShape {
+  static constexpr int ROWS = G / kTmaWarps;                  // rows per warp
+  static constexpr uint32_t TILE = G * kTmaCols * 2;          // fp16 tile bytes
+  static constexpr uint32_t RED_OFF = kTmaStages * TILE;      // [2 parity][2 lo/hi][warps][128] fp16
+  static constexpr uint32_t RED = 2 * 2 * kTmaWarps * kTmaCols * 2;
+  static constexpr uint32_t BAR_OFF = RED_OFF + RED;          // full[S], empty[S], red[2], abort
+  static constexpr uint32_t SMEM = BAR_OFF + 8 * (2 * kTmaStages + 2) + 16 + 128;  // + alignment slack
+};
+
+// Four columns' scale bits, zero bytes, zero points and reciprocals from the
+// group's lo and hi (the rule in the header comment).
+__device__ __forceinline__ void rtn_params4(const float (&lo)[4], const float (&hi)[4], float (&inv)[4],
+                                            float (&zf)[4], uint2& sbits, uint32_t& zbytes) {
+  const __half tiny = __ushort_as_half((unsigned short)1);  // 2^-24, the smallest positive fp16
+  uint32_t sb[2] = {0u, 0u};
+  zbytes = 0;
 #pragma unroll
-  for (int c = 0; c < kCols; ++c) lo[c] = hi[c] = 0.f;
-  if (active) {
+  for (int c = 0; c < 4; ++c) {
+    float r = hi[c] - lo[c];
+    if (r == 0.f) r = 15.f;
+    __half sh = __float2half_rn(__fdiv_rn(r, 15.f));
+    if (__half2float(sh) < __half2float(tiny)) sh = tiny;
+    const float sf = __half2float(sh);
+    zf[c] = fminf(fmaxf(rintf(__fdiv_rn(-lo[c], sf)), 0.f), 15.f);
+    inv[c] = __fdiv_rn(1.f, sf);
+    sb[c >> 1] |= (uint32_t)__half_as_ushort(sh) << (16 * (c & 1));
+    zbytes |= (uint32_t)zf[c] << (8 * c);
+  }
+  sbits = make_uint2(sb[0], sb[1]);
+}
+
+// Four codes (the magic-constant rounding of rtn_codes) as the bytes of a word.
+__device__ __forceinline__ uint32_t rtn_codes4(const float (&f)[4], const float (&inv)[4], const float (&zf)[4]) {
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+  uint32_t u[4];
 #pragma unroll
-    for (int i = 0; i < R; ++i) v[i] = w[(size_t)(ty + kRegSlices * i) * N8];
+  for (int c = 0; c < 4; ++c) {
+    const float t = __fadd_rn(__fadd_rn(__fmul_rn(f[c], inv[c]), kMagic), zf[c]);
+    u[c] = __float_as_uint(fminf(fmaxf(t, kMagic), kMagic + 15.f));
+  }
+  return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u);
+}
+
+__device__ __forceinline__ void unpack4(const uint2 v, float (&f)[4]) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_constant__ CUtensorMap tmW, int N,
+                                                                 int tiles, int NB, uint8_t* __restrict__ q,
+                                                                 uint8_t* __restrict__ z, __half* __restrict__ s) {
+  using SH = RtnTmaShape<G>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 127u) & ~127u;
+  uint8_t* smem = smem_raw + (base - raw_base);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int my_tiles = (int)blockIdx.x < tiles ? (tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const uint32_t bar0 = base + SH::BAR_OFF;
+  auto full = [&](int i) { return bar0 + 8 * i; };
+  auto empty = [&](int i) { return bar0 + 8 * (kTmaStages + i); };
+  auto red_bar = [&](int i) { return bar0 + 8 * (2 * kTmaStages + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SH::BAR_OFF + 8 * (2 * kTmaStages + 2));
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTmaStages; ++i) {
+      mbar_init(full(i), 1);
+      mbar_init(empty(i), kTmaWarps);
+    }
+    mbar_init(red_bar(0), kTmaWarps);
+    mbar_init(red_bar(1), kTmaWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+    launch_dependents();  // the next grid may start; it waits for this one before reading q, z, s
+  }
+  __syncthreads();
+
+  if (warp == kTmaWarps) {
+    // ---------------- producer: one TMA copy per tile ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmW);
+      grid_dependency_wait();  // W may be written by the preceding grid
+      int issued = 0;
+      for (int it = 0; it < my_tiles; ++it) {
+        const int slot = it % kTmaStages;
+        if (it >= kTmaStages &&
+            !mbar_wait(empty(slot), (uint32_t)(it / kTmaStages - 1) & 1u, abort_flag, &s_err_rtn))
+          break;
+        const int t = (int)blockIdx.x + it * (int)gridDim.x;
+        mbar_expect_tx(full(slot), SH::TILE);
+        tma_load_2d(base + slot * SH::TILE, &tmW, (t % NB) * kTmaCols, (t / NB) * G, full(slot));
+        ++issued;
+      }
+      // Never leave with copies in flight into this CTA's shared memory.
+      for (int i = max(0, issued - kTmaStages); i < issued; ++i) {
+        const uint32_t bar = full(i % kTmaStages), parity = (uint32_t)(i / kTmaStages) & 1u;
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(bar, parity))
+          if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(&s_err_rtn, kErrTimeout);
+            break;
+          }
+      }
+    }
+    return;
+  }
+
+  // ---------------- quantising warps ----------------
+  constexpr int R = SH::ROWS;
+  __half* red = reinterpret_cast<__half*>(smem + SH::RED_OFF);
+  for (int it = 0; it < my_tiles; ++it) {
+    const int slot = it % kTmaStages;
+    if (!mbar_wait(full(slot), (uint32_t)(it / kTmaStages) & 1u, abort_flag, &s_err_rtn)) break;
+    const uint8_t* tile = smem + slot * SH::TILE;
+    uint2 v[R];
 #pragma unroll
-    for (int i = 0; i < R; ++i) {
-      float f[kCols];
-      unpack8(v[i], f);
+    for (int r = 0; r < R; ++r)
+      v[r] = *reinterpret_cast<const uint2*>(tile + (warp * R + r) * (kTmaCols * 2) + lane * 8);
+    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kCols; ++c) {
+    for (int r = 0; r < R; ++r) {
+      float f[4];
+      unpack4(v[r], f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         lo[c] = fminf(lo[c], f[c]);
         hi[c] = fmaxf(hi[c], f[c]);
       }
     }
-  }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(slot));  // the rows are in registers: the slot may refill
+    // lo and hi are fp16 values (or 0): exact in fp16
+    const int par = it & 1;
+    __half* red_lo = red + ((par * 2 + 0) * kTmaWarps) * kTmaCols;
+    __half* red_hi = red + ((par * 2 + 1) * kTmaWarps) * kTmaCols;
+    const __half2 l01 = __floats2half2_rn(lo[0], lo[1]), l23 = __floats2half2_rn(lo[2], lo[3]);
+    const __half2 h01 = __floats2half2_rn(hi[0], hi[1]), h23 = __floats2half2_rn(hi[2], hi[3]);
+    *reinterpret_cast<uint2*>(red_lo + warp * kTmaCols + 4 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+    *reinterpret_cast<uint2*>(red_hi + warp * kTmaCols + 4 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_bar(par));
+    if (!mbar_wait(red_bar(par), (uint32_t)(it >> 1) & 1u, abort_flag, &s_err_rtn)) break;
 #pragma unroll
-  for (int c = 0; c < kCols; ++c) {
-    s_lo[ty][tx][c] = lo[c];
-    s_hi[ty][tx][c] = hi[c];
-  }
-  __syncthreads();
-  if (!active) return;
+    for (int w = 0; w < kTmaWarps; ++w) {
+      float f[4];
+      unpack4(*reinterpret_cast<const uint2*>(red_lo + w * kTmaCols + 4 * lane), f);
 #pragma unroll
-  for (int c = 0; c < kCols; ++c)
+      for (int c = 0; c < 4; ++c) lo[c] = fminf(lo[c], f[c]);
+      unpack4(*reinterpret_cast<const uint2*>(red_hi + w * kTmaCols + 4 * lane), f);
 #pragma unroll
-    for (int y = 0; y < kRegSlices; ++y) {
-      lo[c] = fminf(lo[c], s_lo[y][tx][c]);
-      hi[c] = fmaxf(hi[c], s_hi[y][tx][c]);
+      for (int c = 0; c < 4; ++c) hi[c] = fmaxf(hi[c], f[c]);
     }
-  float inv[kCols], zf[kCols];
-  uint32_t sbits[4], zlo, zhi;
-  rtn_params(lo, hi, inv, zf, sbits, zlo, zhi);
-  uint2* qr = q + (size_t)grp * G * N8 + c8;
+    float inv[4], zf[4];
+    uint2 sbits;
+    uint32_t zbytes;
+    rtn_params4(lo, hi, inv, zf, sbits, zbytes);
+    const int t = (int)blockIdx.x + it * (int)gridDim.x;
+    const int grp = t / NB, col = (t % NB) * kTmaCols + 4 * lane;
+    if (col < N) {
+      uint8_t* qr = q + ((size_t)grp * G + warp * R) * N + col;
 #pragma unroll
-  for (int i = 0; i < R; ++i) {
-    float f[kCols];
-    unpack8(v[i], f);
-    qr[(size_t)(ty + kRegSlices * i) * N8] = rtn_codes(f, inv, zf);
+      for (int r = 0; r < R; ++r) {
+        float f[4];
+        unpack4(v[r], f);
+        *reinterpret_cast<uint32_t*>(qr + (size_t)r * N) = rtn_codes4(f, inv, zf);
+      }
+      if (warp == 0) {
+        *reinterpret_cast<uint32_t*>(z + (size_t)grp * N + col) = zbytes;
+        *reinterpret_cast<uint2*>(s + (size_t)grp * N + col) = sbits;
+      }
+    }
   }
-  if (ty == 0) {
-    z[(size_t)grp * N8 + c8] = make_uint2(zlo, zhi);
-    s[(size_t)grp * N8 + c8] = make_uint4(sbits[0], sbits[1], sbits[2], sbits[3]);
+}
+
+// Host side of rtn_tma_kernel: the tensor map of W (fp16 [K][N], boxes of
+// 128 columns x G rows, no swizzle) and a persistent launch of at most two
+// CTAs per SM, with programmatic dependent launch.
+template <int G>
+tm_status rtn_tma_launch(const uint16_t* W, int K, int N, uint8_t* q, uint8_t* z, uint16_t* s, cudaStream_t st) {
+  using SH = RtnTmaShape<G>;
+  auto kern = rtn_tma_kernel<G>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM) != cudaSuccess)
+      return TM_ERR_CUDA;
+    attr_done = true;
   }
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return TM_ERR_CUDA;
+  CUtensorMap tm;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTmaCols, (cuuint32_t)G};
+  cuuint32_t es[2] = {1, 1};
+  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t*>(W), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TM_ERR_CUDA;
+  int device = 0, per_sm = 0;
+  if (cudaGetDevice(&device) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, SH::SMEM) != cudaSuccess ||
+      per_sm < 1)
+    return TM_ERR_CUDA;
+  const int NB = (N + kTmaCols - 1) / kTmaCols;
+  const long long tiles_ll = (long long)NB * (K / G);
+  if (tiles_ll > (1ll << 30)) return TM_ERR_UNSUPPORTED;
+  const int tiles = (int)tiles_ll;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(tiles, std::min(per_sm, 2) * num_sms(device)), 1, 1);
+  cfg.blockDim = dim3(kTmaThreads, 1, 1);
+  cfg.dynamicSmemBytes = SH::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm, N, tiles, NB, q, z, reinterpret_cast<__half*>(s)) == cudaSuccess
+             ? TM_OK
+             : TM_ERR_CUDA;
 }
 
 }  // namespace
@@ -221,14 +400,29 @@ extern "C" tm_status tm_quantize_rtn(const uint16_t* W, int K, int N, int g, uin
   auto* qv = reinterpret_cast<uint2*>(q);
   auto* zv = reinterpret_cast<uint2*>(z);
   auto* sv = reinterpret_cast<uint4*>(s);
-  if (g == 128) {
-    rtn_reg_kernel<128><<<grid, kRegThreads, 0, st>>>(Wv, N, qv, zv, sv);
-  } else if (g == 64) {
-    rtn_reg_kernel<64><<<grid, kRegThreads, 0, st>>>(Wv, N, qv, zv, sv);
+  if (g == 128 || g == 64) {
+    const tm_status r = g == 128 ? rtn_tma_launch<128>(W, K, N, q, z, s, st) : rtn_tma_launch<64>(W, K, N, q, z, s, st);
+    if (r != TM_OK) return r;
   } else {
     rtn_kernel<<<grid, kQuantThreads, 0, st>>>(Wv, N, g, qv, zv, sv);
+    if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
   }
-  if (cudaGetLastError() != cudaSuccess) return TM_ERR_CUDA;
   set_launch_count(1);
   return TM_OK;
 }
+
+namespace w4 {
+
+cudaError_t rtn_error_bits(uint32_t* bits, bool clear) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, s_err_rtn, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (clear && v) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(s_err_rtn, &zero, sizeof(zero));
+  }
+  *bits = v;
+  return e;
+}
+
+}  // namespace w4
