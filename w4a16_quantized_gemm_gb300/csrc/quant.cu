@@ -14,11 +14,11 @@
 // HBM-bound: 2 bytes read and 1 byte written per weight.
 // g = 64 and 128 (rtn_tma_kernel): a persistent grid, two CTAs per SM, walks
 // tiles of one group's g rows x 128 columns.  One thread streams the tiles
-// with 2-D TMA copies into a ring of shared-memory slots; eight warps take a
-// tile each, warp w rows w g/8 .. (w + 1) g/8 - 1, lane l columns 4l .. 4l+3,
+// with 2-D TMA copies into a ring of shared-memory slots; eight warps share
+// each tile, warp w rows w g/8 .. (w + 1) g/8 - 1, lane l columns 4l .. 4l+3,
 // loading their rows into registers and releasing the slot at once; the
-// warps' column minima and maxima meet in shared memory (double-buffered
-// by tile parity, behind an mbarrier), and each thread writes its codes as
+// warps' column minima and maxima meet in shared memory, each column's
+// scale and zero are computed once, and each thread writes its codes as
 // 4-byte stores (a warp writes 128 contiguous bytes per row).  Every weight
 // is read from HBM once and the ring keeps copies in flight while the warps
 // compute.  Other group sizes (rtn_kernel, 4 warps, 256 columns per block)
@@ -155,30 +155,23 @@ struct RtnTmaShape {
   static constexpr uint32_t TILE = G * kTmaCols * 2;          // fp16 tile bytes
   static constexpr uint32_t RED_OFF = kTmaStages * TILE;      // [2 parity][2 lo/hi][warps][128] fp16
   static constexpr uint32_t RED = 2 * 2 * kTmaWarps * kTmaCols * 2;
-  static constexpr uint32_t BAR_OFF = RED_OFF + RED;          // full[S], empty[S], red[2], abort
-  static constexpr uint32_t SMEM = BAR_OFF + 8 * (2 * kTmaStages + 2) + 16 + 128;  // + alignment slack
+  static constexpr uint32_t PAR_OFF = RED_OFF + RED;          // [2 parity][2 inv/zero][128] fp32
+  static constexpr uint32_t PAR = 2 * 2 * kTmaCols * 4;
+  static constexpr uint32_t BAR_OFF = PAR_OFF + PAR;          // full[S], empty[S], red[2], par[2], abort
+  static constexpr uint32_t SMEM = BAR_OFF + 8 * (2 * kTmaStages + 4) + 16 + 128;  // + alignment slack
 };
 
-// Four columns' scale bits, zero bytes, zero points and reciprocals from the
-// group's lo and hi (the rule in the header comment).
-__device__ __forceinline__ void rtn_params4(const float (&lo)[4], const float (&hi)[4], float (&inv)[4],
-                                            float (&zf)[4], uint2& sbits, uint32_t& zbytes) {
+// One column's scale, zero point and reciprocal from the group's lo and hi
+// (the rule in the header comment).
+__device__ __forceinline__ void rtn_params1(float lo, float hi, float& inv, float& zf, __half& sh) {
   const __half tiny = __ushort_as_half((unsigned short)1);  // 2^-24, the smallest positive fp16
-  uint32_t sb[2] = {0u, 0u};
-  zbytes = 0;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float r = hi[c] - lo[c];
-    if (r == 0.f) r = 15.f;
-    __half sh = __float2half_rn(__fdiv_rn(r, 15.f));
-    if (__half2float(sh) < __half2float(tiny)) sh = tiny;
-    const float sf = __half2float(sh);
-    zf[c] = fminf(fmaxf(rintf(__fdiv_rn(-lo[c], sf)), 0.f), 15.f);
-    inv[c] = __fdiv_rn(1.f, sf);
-    sb[c >> 1] |= (uint32_t)__half_as_ushort(sh) << (16 * (c & 1));
-    zbytes |= (uint32_t)zf[c] << (8 * c);
-  }
-  sbits = make_uint2(sb[0], sb[1]);
+  float r = hi - lo;
+  if (r == 0.f) r = 15.f;
+  sh = __float2half_rn(__fdiv_rn(r, 15.f));
+  if (__half2float(sh) < __half2float(tiny)) sh = tiny;
+  const float sf = __half2float(sh);
+  zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), 15.f);
+  inv = __fdiv_rn(1.f, sf);
 }
 
 // Four codes (the magic-constant rounding of rtn_codes) as the bytes of a word.
@@ -217,15 +210,18 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
   auto full = [&](int i) { return bar0 + 8 * i; };
   auto empty = [&](int i) { return bar0 + 8 * (kTmaStages + i); };
   auto red_bar = [&](int i) { return bar0 + 8 * (2 * kTmaStages + i); };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SH::BAR_OFF + 8 * (2 * kTmaStages + 2));
+  auto par_bar = [&](int i) { return bar0 + 8 * (2 * kTmaStages + 2 + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SH::BAR_OFF + 8 * (2 * kTmaStages + 4));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTmaStages; ++i) {
       mbar_init(full(i), 1);
       mbar_init(empty(i), kTmaWarps);
     }
-    mbar_init(red_bar(0), kTmaWarps);
-    mbar_init(red_bar(1), kTmaWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(red_bar(i), kTmaWarps);
+      mbar_init(par_bar(i), kTmaWarps);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     launch_dependents();  // the next grid may start; it waits for this one before reading q, z, s
@@ -263,8 +259,14 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
   }
 
   // ---------------- quantising warps ----------------
+  // Per tile: rows into registers and the slot released; column minima and
+  // maxima per warp (half2, exact) into shared memory; warp w then finishes
+  // columns 16 w .. 16 w + 15 (one per lane: the three divisions of the rule
+  // once per column) and publishes 1/s and z; every lane codes its 4 columns.
+  // Both exchanges are double-buffered by tile parity behind mbarriers.
   constexpr int R = SH::ROWS;
   __half* red = reinterpret_cast<__half*>(smem + SH::RED_OFF);
+  float* par = reinterpret_cast<float*>(smem + SH::PAR_OFF);
   for (int it = 0; it < my_tiles; ++it) {
     const int slot = it % kTmaStages;
     if (!mbar_wait(full(slot), (uint32_t)(it / kTmaStages) & 1u, abort_flag, &s_err_rtn)) break;
@@ -273,59 +275,64 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
 #pragma unroll
     for (int r = 0; r < R; ++r)
       v[r] = *reinterpret_cast<const uint2*>(tile + (warp * R + r) * (kTmaCols * 2) + lane * 8);
-    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(slot));  // the rows are in registers: the slot may refill
+    const __half2 zero2 = __float2half2_rn(0.f);
+    __half2 lo01 = zero2, lo23 = zero2, hi01 = zero2, hi23 = zero2;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float f[4];
-      unpack4(v[r], f);
+      const __half2 a = *reinterpret_cast<const __half2*>(&v[r].x), b = *reinterpret_cast<const __half2*>(&v[r].y);
+      lo01 = __hmin2(lo01, a);
+      hi01 = __hmax2(hi01, a);
+      lo23 = __hmin2(lo23, b);
+      hi23 = __hmax2(hi23, b);
+    }
+    const int pb = it & 1;
+    __half* red_lo = red + ((pb * 2 + 0) * kTmaWarps) * kTmaCols;
+    __half* red_hi = red + ((pb * 2 + 1) * kTmaWarps) * kTmaCols;
+    *reinterpret_cast<uint2*>(red_lo + warp * kTmaCols + 4 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&lo01), *reinterpret_cast<const uint32_t*>(&lo23));
+    *reinterpret_cast<uint2*>(red_hi + warp * kTmaCols + 4 * lane) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&hi01), *reinterpret_cast<const uint32_t*>(&hi23));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(red_bar(pb));
+    if (!mbar_wait(red_bar(pb), (uint32_t)(it >> 1) & 1u, abort_flag, &s_err_rtn)) break;
+    const int t = (int)blockIdx.x + it * (int)gridDim.x;
+    const int grp = t / NB, col0 = (t % NB) * kTmaCols;
+    float* p_inv = par + (pb * 2 + 0) * kTmaCols;
+    float* p_zf = par + (pb * 2 + 1) * kTmaCols;
+    if (lane < 16) {
+      const int c = 16 * warp + lane;
+      __half lo = red_lo[c], hi = red_hi[c];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        lo[c] = fminf(lo[c], f[c]);
-        hi[c] = fmaxf(hi[c], f[c]);
+      for (int w = 1; w < kTmaWarps; ++w) {
+        lo = __hmin(lo, red_lo[w * kTmaCols + c]);
+        hi = __hmax(hi, red_hi[w * kTmaCols + c]);
+      }
+      float inv, zf;
+      __half sh;
+      rtn_params1(__half2float(lo), __half2float(hi), inv, zf, sh);
+      p_inv[c] = inv;
+      p_zf[c] = zf;
+      if (col0 + c < N) {
+        z[(size_t)grp * N + col0 + c] = (uint8_t)zf;
+        s[(size_t)grp * N + col0 + c] = sh;
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty(slot));  // the rows are in registers: the slot may refill
-    // lo and hi are fp16 values (or 0): exact in fp16
-    const int par = it & 1;
-    __half* red_lo = red + ((par * 2 + 0) * kTmaWarps) * kTmaCols;
-    __half* red_hi = red + ((par * 2 + 1) * kTmaWarps) * kTmaCols;
-    const __half2 l01 = __floats2half2_rn(lo[0], lo[1]), l23 = __floats2half2_rn(lo[2], lo[3]);
-    const __half2 h01 = __floats2half2_rn(hi[0], hi[1]), h23 = __floats2half2_rn(hi[2], hi[3]);
-    *reinterpret_cast<uint2*>(red_lo + warp * kTmaCols + 4 * lane) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
-    *reinterpret_cast<uint2*>(red_hi + warp * kTmaCols + 4 * lane) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
-    __syncwarp();
-    if (lane == 0) mbar_arrive(red_bar(par));
-    if (!mbar_wait(red_bar(par), (uint32_t)(it >> 1) & 1u, abort_flag, &s_err_rtn)) break;
-#pragma unroll
-    for (int w = 0; w < kTmaWarps; ++w) {
-      float f[4];
-      unpack4(*reinterpret_cast<const uint2*>(red_lo + w * kTmaCols + 4 * lane), f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) lo[c] = fminf(lo[c], f[c]);
-      unpack4(*reinterpret_cast<const uint2*>(red_hi + w * kTmaCols + 4 * lane), f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) hi[c] = fmaxf(hi[c], f[c]);
-    }
-    float inv[4], zf[4];
-    uint2 sbits;
-    uint32_t zbytes;
-    rtn_params4(lo, hi, inv, zf, sbits, zbytes);
-    const int t = (int)blockIdx.x + it * (int)gridDim.x;
-    const int grp = t / NB, col = (t % NB) * kTmaCols + 4 * lane;
+    if (lane == 0) mbar_arrive(par_bar(pb));
+    if (!mbar_wait(par_bar(pb), (uint32_t)(it >> 1) & 1u, abort_flag, &s_err_rtn)) break;
+    const int col = col0 + 4 * lane;
     if (col < N) {
+      const float4 i4 = *reinterpret_cast<const float4*>(p_inv + 4 * lane);
+      const float4 z4 = *reinterpret_cast<const float4*>(p_zf + 4 * lane);
+      const float inv[4] = {i4.x, i4.y, i4.z, i4.w}, zf[4] = {z4.x, z4.y, z4.z, z4.w};
       uint8_t* qr = q + ((size_t)grp * G + warp * R) * N + col;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float f[4];
         unpack4(v[r], f);
         *reinterpret_cast<uint32_t*>(qr + (size_t)r * N) = rtn_codes4(f, inv, zf);
-      }
-      if (warp == 0) {
-        *reinterpret_cast<uint32_t*>(z + (size_t)grp * N + col) = zbytes;
-        *reinterpret_cast<uint2*>(s + (size_t)grp * N + col) = sbits;
       }
     }
   }
@@ -355,11 +362,16 @@ tm_status rtn_tma_launch(const uint16_t* W, int K, int N, uint8_t* q, uint8_t* z
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return TM_ERR_CUDA;
-  int device = 0, per_sm = 0;
-  if (cudaGetDevice(&device) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, SH::SMEM) != cudaSuccess ||
-      per_sm < 1)
-    return TM_ERR_CUDA;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= 64) return TM_ERR_CUDA;
+  static int per_sm_cache[64] = {};  // resident CTAs per SM, per device (0 = not yet queried)
+  int per_sm = per_sm_cache[device];
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTmaThreads, SH::SMEM) != cudaSuccess ||
+        per_sm < 1)
+      return TM_ERR_CUDA;
+    per_sm_cache[device] = per_sm;
+  }
   const int NB = (N + kTmaCols - 1) / kTmaCols;
   const long long tiles_ll = (long long)NB * (K / G);
   if (tiles_ll > (1ll << 30)) return TM_ERR_UNSUPPORTED;
