@@ -44,7 +44,8 @@ WORKLOADS = {
                 "name": "llama3-8b prefill linears: qkv/o_proj/gate_up/down x M in {128,1024,4096}, g=128"},
 }
 KERNEL_SOURCES = {"decode": ["decode.cu", "tm_common.cuh"], "tc": ["tc.cu", "tm_common.cuh"],
-                  "kv": ["kv.cu", "tm_common.cuh"], "w8": ["w8a8.cu", "tm_common.cuh"]}
+                  "kv": ["kv.cu", "tm_common.cuh"], "w8": ["w8a8.cu", "tm_common.cuh"],
+                  "rtn": ["quant.cu", "tm_common.cuh"]}
 
 
 # ----------------------------------------------------------------- helpers ---
@@ -639,8 +640,12 @@ def run_rtn(args, rank, world, local):
                    "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (698 MB of fp16 weights per step)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "peak_source": peaks["source"], "kernel": "rtn_tma_kernel"},
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": read_traffic("rtn", "llama3_8b_rtn"),
+                     "peak_source": peaks["source"], "kernel": "rtn_tma_kernel",
+                     "basis": "algorithmic bytes of the step's four launches / mean step time (CUDA events "
+                              "around graph replays); traffic = DRAM bytes per launch, the mean over the "
+                              "step's four launches"},
         "gpu_launches": len(layers) * args.steps, "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
     }
     if rank == 0:
