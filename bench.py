@@ -871,6 +871,9 @@ def run_w8a8(args, rank, world, local, prefill=False):
     binding.load()
     peaks = load_peaks()
     Ms = (128, 1024, 4096) if prefill else (1, 8, 16, 32)
+    # the activation codes: fp16 integers (TMA-staged X, tm_w8a8_gemm_f16) for
+    # prefill, int8 (the decode kernel's operand) for decode, unless forced
+    codes = args.w8_codes if args.w8_codes != "auto" else ("f16" if prefill else "int8")
     host = {}
     items = []
     for name in ("qkv", "o_proj", "gate_up", "down"):
@@ -884,7 +887,8 @@ def run_w8a8(args, rank, world, local, prefill=False):
             X = torch.from_numpy(synth.activations(M, K, tag=f"/w8/{name}/M{M}").view(np.uint16)).to(device)
             X = X.view(torch.float16)
             items.append({"name": name, "M": M, "K": K, "N": N, "w": binding.pack_w8(qd, sd), "X": X,
-                          "xq": torch.empty((M, K), dtype=torch.int8, device=device),
+                          "xq": torch.empty((M, K), dtype=torch.int8 if codes == "int8" else torch.float16,
+                                            device=device),
                           "sx": torch.empty((M,), dtype=torch.float32, device=device),
                           "Y": torch.empty((M, N), dtype=torch.float16, device=device),
                           "bytes": w8a8_bytes(M, K, N),
@@ -897,8 +901,12 @@ def run_w8a8(args, rank, world, local, prefill=False):
 
     def launch_all(st):
         for it in items:
-            binding.w8a8_quantize_act(it["X"], out=(it["xq"], it["sx"]), stream=st)
-            binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
+            if codes == "int8":
+                binding.w8a8_quantize_act(it["X"], out=(it["xq"], it["sx"]), stream=st)
+                binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
+            else:
+                binding.w8a8_quantize_act_f16(it["X"], out=(it["xq"], it["sx"]), stream=st)
+                binding.w8a8_gemm_f16(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
 
     with torch.cuda.stream(stream):
         launch_all(stream)
@@ -965,6 +973,7 @@ def run_w8a8(args, rank, world, local, prefill=False):
         "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"w8a8{'_prefill' if prefill else ''}: qkv, o_proj, gate_up, down x M",
+                   "activation_codes": codes,
                    "launches_per_step": 2 * len(items), "bytes_per_step": step_bytes, "flops_per_step": step_flops,
                    "l2": f"each GEMM has its own packed weights ({weight_bytes / 1e6:.0f} MB per step > 129 MB L2)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
@@ -1045,6 +1054,8 @@ def main(argv=None):
                    default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--w8-codes", choices=["auto", "int8", "f16"], default="auto",
+                   help="W8A8 activation codes: int8 or fp16 integers (auto: fp16 for prefill, int8 for decode)")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
     p.add_argument("--single", default=None, help="M,K,N,g: one GEMM 15 times, cold L2 (for ncu captures)")
     p.add_argument("--path", type=int, default=0,

@@ -95,6 +95,29 @@ tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p,
 tm_status tm_w8a8_gemm_ex(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
                           int tile_m, void* stream);
 
+/*
+ * tm_w8a8_quantize_act with the codes written as exact fp16 integers
+ * (-127..127) instead of int8: the X operand of tm_w8a8_gemm_f16.
+ *   X   : device fp16 bits [M][K] row-major, 16-byte aligned; K % 16 == 0
+ *   xq16: device fp16 bits [M][K], 16-byte aligned;  sx: device fp32 [M], 4-byte aligned
+ * Same codes and scales as tm_w8a8_quantize_act, bit for bit; one launch.
+ */
+tm_status tm_w8a8_quantize_act_f16(const uint16_t* X, int M, int K, uint16_t* xq16, float* sx, void* stream);
+
+/*
+ * The product of tm_w8a8_gemm with the codes as fp16 integers (from
+ * tm_w8a8_quantize_act_f16), for the tensor-memory kernel: X is copied into
+ * shared memory by TMA as the MMA's B operand with no conversion, so the
+ * kernel's converter warps handle the weights only (the int8 form converts
+ * both, and its shared-memory traffic per 128-k block is ~1.4x higher).
+ * Every M runs the tensor-memory kernel (use tm_w8a8_gemm with int8 codes for
+ * decode, M <= 32).  split_k and tile_m as in tm_w8a8_gemm_ex; for M > 32 the
+ * result equals tm_w8a8_gemm_ex's bit for bit (same products, same order).
+ *   xq16: device fp16 [M][K], 16-byte aligned;  sx: fp32 [M];  Y: fp16 [M][N], 16-byte aligned
+ */
+tm_status tm_w8a8_gemm_f16(const uint16_t* xq16, const float* sx, const tm_w8_packed* p, void* Y, int M,
+                           int split_k, int tile_m, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -160,3 +160,17 @@ def test_host_buffer_entry_points_reject_bad_arguments(lib):
     ms = (ctypes.c_int * 2)(1, 1)
     assert lib.tm_w4a16_gemm_host_batch(2, ps, ms, a16, a16, a16, odd, None) == INVALID    # null handle
     assert lib.tm_last_launch_count() == 0
+
+
+def test_w8a8_f16_entry_points_reject_bad_host_arguments(lib):
+    a16, odd = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 2)
+    INVALID, ALIGN, OK = 1, 2, 0
+    assert lib.tm_w8a8_quantize_act_f16(None, 1, 128, a16, a16, None) == INVALID
+    assert lib.tm_w8a8_quantize_act_f16(a16, 1, 100, a16, a16, None) == INVALID       # K % 16
+    assert lib.tm_w8a8_quantize_act_f16(a16, 1, 128, odd, a16, None) == ALIGN
+    assert lib.tm_w8a8_quantize_act_f16(a16, 0, 128, a16, a16, None) == OK            # no rows
+    assert lib.tm_w8a8_gemm_f16(None, a16, a16, a16, 64, 0, 0, None) == INVALID
+    assert lib.tm_w8a8_gemm_f16(a16, a16, a16, a16, 64, 3, 0, None) == INVALID         # split
+    assert lib.tm_w8a8_gemm_f16(a16, a16, a16, a16, 64, 0, 32, None) == INVALID        # tile_m
+    assert lib.tm_w8a8_gemm_f16(odd, a16, a16, a16, 64, 0, 0, None) == ALIGN
+    assert lib.tm_w8a8_gemm_f16(a16, a16, a16, a16, 0, 0, 0, None) == OK               # M = 0

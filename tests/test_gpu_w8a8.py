@@ -184,3 +184,88 @@ def test_gpu_quantisers_pack_gemm_pipeline():
     qx0, sx0 = w8.quantize_act(X)
     ref = w8.gemm(qx0, sx0, q0, s0)
     assert oracle.rel_max_err(Y.float().cpu().numpy().astype(np.float64), ref) <= TOL
+
+
+# ---- the codes as fp16 integers (tm_w8a8_quantize_act_f16, tm_w8a8_gemm_f16) ----
+
+@pytest.mark.parametrize("M", [1, 33, 300])
+@pytest.mark.parametrize("K", [16, 1040, 4096])
+def test_quantize_act_f16_bit_exact(M, K):
+    """The fp16 codes are the oracle's integer codes exactly, the scales bit for bit."""
+    X = _acts(M, K, tag="q16")
+    xq16, sx = binding.w8a8_quantize_act_f16(torch.from_numpy(X.view(np.uint16)).cuda().view(torch.float16))
+    torch.cuda.synchronize()
+    q0, s0 = w8.quantize_act(X)
+    assert np.array_equal(sx.cpu().numpy().view(np.uint32), s0.view(np.uint32))
+    codes = xq16.float().cpu().numpy()
+    assert np.array_equal(codes, q0.astype(np.float32))
+
+
+def _check_f16(M, K, N, split=0, tile_m=0, rows=None):
+    q, s = _weights(K, N)
+    X = _acts(M, K)
+    qx, sx = w8.quantize_act(X)
+    xq16 = torch.from_numpy(qx.astype(np.float16)).cuda()
+    sxd = torch.from_numpy(sx).cuda()
+    Y = binding.w8a8_gemm_f16(xq16, sxd, _packed(K, N), split=split, tile_m=tile_m)
+    torch.cuda.synchronize()
+    assert binding.device_error(clear=True) == 0
+    rows = sample_rows(M) if rows is None else rows
+    ref = w8.gemm(qx, sx, q, s, rows=rows)
+    got = Y[torch.tensor(rows, device=Y.device)].float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    bound = np.abs(ref) * (2.0 ** -11 + 2.0 ** -20) + 2.0 ** -24 + 2.0 ** -22 * np.abs(ref).max()
+    assert np.all(np.abs(got - ref) <= bound), float(np.max(np.abs(got - ref) / bound))
+    return Y, torch.from_numpy(qx).cuda(), sxd
+
+
+@pytest.mark.parametrize("tile_m", [64, 128, 256])
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("M", [40, 129, 300])
+def test_gemm_f16_tiles_split_ragged_equal_to_int8_path(tile_m, split, M):
+    """Every row tile and split on a partial last 128-k block, a partial
+    128-column block and a partial row tile: within the bound of the oracle,
+    and bit for bit the int8 path's result (same products, same order)."""
+    Y16, xq, sx = _check_f16(M, 1040, 272, split=split, tile_m=tile_m)
+    Y8 = binding.w8a8_gemm(xq, sx, _packed(1040, 272), split=split, tile_m=tile_m)
+    torch.cuda.synchronize()
+    assert torch.equal(Y16.view(torch.int16), Y8.view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [1, 7, 32, 33, 1024])
+def test_gemm_f16_auto(M):
+    """Small M too (the tensor-memory kernel with 64-row tiles)."""
+    _check_f16(M, 2048, 1024)
+
+
+def test_gemm_f16_llama3_8b_prefill_sampled_rows():
+    K, N = synth.LLAMA3_8B["gate_up"]
+    _check_f16(4096, K, N, rows=[0, 1, 2, 255, 256, 2047, 4095])
+
+
+def test_f16_pipeline_gpu_quantiser():
+    K, N, M = 2048, 512, 200
+    q, s = _weights(K, N)
+    X = _acts(M, K, tag="pipe16")
+    xq16, sx = binding.w8a8_quantize_act_f16(torch.from_numpy(X.view(np.uint16)).cuda().view(torch.float16))
+    Y = binding.w8a8_gemm_f16(xq16, sx, _packed(K, N))
+    torch.cuda.synchronize()
+    q0, s0 = w8.quantize_act(X)
+    ref = w8.gemm(q0, s0, q, s)
+    assert oracle.rel_max_err(Y.float().cpu().numpy().astype(np.float64), ref) <= TOL
+
+
+def test_f16_rejects_bad_arguments():
+    w = _packed(1024, 512)
+    xq = torch.zeros((40, 1024), dtype=torch.float16, device="cuda")
+    sx = torch.ones(40, dtype=torch.float32, device="cuda")
+    with pytest.raises(binding.TMError) as e:
+        binding.w8a8_gemm_f16(xq, sx, w, tile_m=96)
+    assert e.value.status == 1
+    buf = torch.zeros(40 * 1024 + 16, dtype=torch.float16, device="cuda")
+    with pytest.raises(binding.TMError) as e:
+        binding.w8a8_gemm_f16(buf[4:4 + 40 * 1024].view(40, 1024), sx, w)
+    assert e.value.status == 2
+    with pytest.raises(binding.TMError) as e:
+        binding.w8a8_quantize_act_f16(torch.zeros((4, 1000), dtype=torch.float16, device="cuda"))
+    assert e.value.status == 1

@@ -24,7 +24,8 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_last_launch_count", "tm_quantize_rtn", "tm_w4a16_gemm_silu_mul", "tm_selftest_wait_timeout",
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
            "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
-           "tm_w8_quantize_weight", "tm_kv_append", "tm_w4a16_gemm_host", "tm_w4a16_gemm_host_batch")
+           "tm_w8_quantize_weight", "tm_kv_append", "tm_w4a16_gemm_host", "tm_w4a16_gemm_host_batch",
+           "tm_w8a8_quantize_act_f16", "tm_w8a8_gemm_f16")
 
 
 class TMError(RuntimeError):
@@ -116,6 +117,10 @@ def load(path: Optional[str] = None):
     lib.tm_w8_quantize_weight.argtypes = [vp, ci, ci, vp, vp, vp]
     lib.tm_w8a8_gemm_ex.restype = ci
     lib.tm_w8a8_gemm_ex.argtypes = [vp, vp, vp, vp, ci, ci, ci, vp]
+    lib.tm_w8a8_quantize_act_f16.restype = ci
+    lib.tm_w8a8_quantize_act_f16.argtypes = [vp, ci, ci, vp, vp, vp]
+    lib.tm_w8a8_gemm_f16.restype = ci
+    lib.tm_w8a8_gemm_f16.argtypes = [vp, vp, vp, vp, ci, ci, ci, vp]
     _lib = lib
     return lib
 
@@ -488,6 +493,26 @@ def w8a8_quantize_act(X: torch.Tensor, out: Optional[tuple] = None, stream: Opti
     return xq, sx
 
 
+def w8a8_quantize_act_f16(X: torch.Tensor, out: Optional[tuple] = None, stream: Optional[torch.cuda.Stream] = None):
+    """tm_w8a8_quantize_act_f16: the same per-token codes as exact fp16 integers:
+    returns (xq16 fp16 [M][K], sx fp32 [M]), into `out` when given."""
+    if X.dim() != 2 or X.dtype != torch.float16:
+        raise ValueError("X must be fp16 [M][K]")
+    M, K = X.shape
+    if out is None:
+        xq = torch.empty((M, K), dtype=torch.float16, device=X.device)
+        sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    else:
+        xq, sx = out
+        if tuple(xq.shape) != (M, K) or tuple(sx.shape) != (M,):
+            raise ValueError("out must be (fp16 [M][K], fp32 [M])")
+    st = stream if stream is not None else torch.cuda.current_stream(X.device)
+    _check(load().tm_w8a8_quantize_act_f16(_dev(X, torch.float16, "X"), M, K, _dev(xq, torch.float16, "xq16"),
+                                           _dev(sx, torch.float32, "sx"), ctypes.c_void_p(st.cuda_stream)),
+           "tm_w8a8_quantize_act_f16")
+    return xq, sx
+
+
 def w8_quantize_weight(W: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
     """Per-output-channel int8 quantisation of fp16 W [K][N] on the GPU (see
     tm_w8_quantize_weight): returns (q int8 [K][N], sw fp32 [N]), the inputs of
@@ -565,4 +590,24 @@ def w8a8_gemm(xq: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[tor
     _check(load().tm_w8a8_gemm_ex(_dev(xq, torch.int8, "xq"), _dev(sx, torch.float32, "sx"), w.handle,
                                   _dev(out, torch.float16, "out"), M, split, tile_m, ctypes.c_void_p(st.cuda_stream)),
            "tm_w8a8_gemm_ex")
+    return out
+
+
+def w8a8_gemm_f16(xq16: torch.Tensor, sx: torch.Tensor, w: W8Packed, out: Optional[torch.Tensor] = None,
+                  split: int = 0, tile_m: int = 0, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """tm_w8a8_gemm_f16: the product with the codes as fp16 integers [M][K]
+    (from w8a8_quantize_act_f16), on the tensor-memory kernel for every M."""
+    if xq16.dim() != 2 or xq16.shape[1] != w.K:
+        raise ValueError("xq16 must be fp16 [M][K]")
+    M = xq16.shape[0]
+    if tuple(sx.shape) != (M,):
+        raise ValueError("sx must be fp32 [M]")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float16, device=xq16.device)
+    if tuple(out.shape) != (M, w.N):
+        raise ValueError("out must be fp16 [M][N]")
+    st = stream if stream is not None else torch.cuda.current_stream(xq16.device)
+    _check(load().tm_w8a8_gemm_f16(_dev(xq16, torch.float16, "xq16"), _dev(sx, torch.float32, "sx"), w.handle,
+                                   _dev(out, torch.float16, "out"), M, split, tile_m, ctypes.c_void_p(st.cuda_stream)),
+           "tm_w8a8_gemm_f16")
     return out

@@ -66,8 +66,11 @@ constexpr uint32_t kW8SmemMax = 227 * 1024;
 // Under programmatic dependent launch the next grid (the GEMM, which streams
 // its weights first) may start at once; X is read and xq, sx written only
 // after the preceding grid finished.
+// F16: the codes written as exact fp16 integers (for the tensor-memory
+// kernel's X path), else as int8.
+template <bool F16>
 __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restrict__ X, int K,
-                                                            int8_t* __restrict__ q, float* __restrict__ sx) {
+                                                            void* __restrict__ q, float* __restrict__ sx) {
   __shared__ float red[8];
   launch_dependents();
   grid_dependency_wait();
@@ -94,19 +97,32 @@ __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restr
   const float s = a == 0.f ? 1.f : __fdiv_rn(a, 127.f);
   const float inv = __fdiv_rn(1.f, s);
   if (threadIdx.x == 0) sx[m] = s;
-  uint2* out = reinterpret_cast<uint2*>(q + (size_t)m * K);
   for (int i = threadIdx.x; i < nv; i += 256) {
     const uint4 v = row[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t b[8];
+    float c[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-      b[2 * e] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.x, inv)), -127.f), 127.f) & 0xFFu;
-      b[2 * e + 1] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.y, inv)), -127.f), 127.f) & 0xFFu;
+      c[2 * e] = fminf(fmaxf(rintf(__fmul_rn(f.x, inv)), -127.f), 127.f);
+      c[2 * e + 1] = fminf(fmaxf(rintf(__fmul_rn(f.y, inv)), -127.f), 127.f);
     }
-    out[i] = make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                        b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+    if (F16) {
+      // integers of magnitude <= 127: exact in fp16
+      uint32_t h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __half2 t = __floats2half2_rn(c[2 * e], c[2 * e + 1]);
+        h[e] = *reinterpret_cast<const uint32_t*>(&t);
+      }
+      reinterpret_cast<uint4*>(static_cast<__half*>(q) + (size_t)m * K)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+      uint32_t b[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) b[e] = (uint32_t)(int)c[e] & 0xFFu;
+      reinterpret_cast<uint2*>(static_cast<int8_t*>(q) + (size_t)m * K)[i] =
+          make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+    }
   }
 }
 
@@ -456,13 +472,16 @@ __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_const
 constexpr int kW8TcThreads = 320;
 constexpr int kW8TcConv = 2;  // converted slots (tensor-memory A + fp16 X)
 
-template <int BT>
+template <int BT, bool XH>
 struct W8TcShape {
   static constexpr uint32_t W_BYTES = 128 * 128;  // one 128-k block of 128 weight rows
   static constexpr uint32_t XR_BYTES = BT * 128;  // one 128-k block of BT int8 rows
-  static constexpr uint32_t SLOT = W_BYTES + XR_BYTES;
-  static constexpr uint32_t XF_UNIT = BT * 128;  // fp16 X, one 64-k unit
+  static constexpr uint32_t XF_UNIT = BT * 128;   // fp16 X, one 64-k unit
   static constexpr uint32_t XF_SLOT = 2 * XF_UNIT;
+  // XH: X arrives as fp16 codes (two 64-k units) in the ring slot itself;
+  // otherwise as int8, converted into XF_SLOT-sized buffers of their own.
+  static constexpr uint32_t SLOT = W_BYTES + (XH ? XF_SLOT : XR_BYTES);
+  static constexpr uint32_t CONV_SLOTS = XH ? 0 : kW8TcConv;  // converted X buffers
   static constexpr uint32_t A_COLS = 64;  // 8 slices of 16 k, 8 columns each
   static constexpr uint32_t A_COL = BT;   // A slots right after the accumulator columns
   static constexpr uint32_t TMEM_COLS = BT + kW8TcConv * A_COLS <= 256 ? 256 : 512;
@@ -487,11 +506,11 @@ __device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
 }
 
-template <int BT>
+template <int BT, bool XH>
 __global__ void __launch_bounds__(kW8TcThreads, 1)
     w8tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const W8TcParams P) {
-  using SH = W8TcShape<BT>;
+  using SH = W8TcShape<BT, XH>;
   constexpr int SC = kW8TcConv;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -521,7 +540,9 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
       mbar_init(fullA(s), 1);
-      mbar_init(emptyA(s), 8);
+      // XH: the slot holds the MMA's B operand and is freed by its commit;
+      // otherwise by the eight converter warps
+      mbar_init(emptyA(s), XH ? 1 : 8);
     }
     for (int s = 0; s < SC; ++s) {
       mbar_init(fullC(s), 8);
@@ -548,7 +569,14 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
       prefetch_tmap(&tmW);
       auto issue_w = [&](int i, int s) { tma_load_3d(base + s * SH::SLOT, &tmW, 0, nt0 * 16, kb0 + i, fullA(s)); };
       auto issue_x = [&](int i, int s) {
-        tma_load_2d(base + s * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(s));
+        if (XH) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            tma_load_2d(base + s * SH::SLOT + SH::W_BYTES + u * SH::XF_UNIT, &tmX, (kb0 + i) * 128 + 64 * u, m0,
+                        fullA(s));
+        } else {
+          tma_load_2d(base + s * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(s));
+        }
       };
       const int first = min(nkb, SA);
       for (int i = 0; i < first; ++i) {
@@ -575,10 +603,13 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, BT);
       for (int i = 0; i < nkb; ++i) {
-        const int sc = i % SC;
+        const int sc = i % SC, s = i % SA;
         if (!mbar_wait(fullC(sc), (uint32_t)(i / SC) & 1u, abort_flag, &s_err_w8)) break;
+        // XH: B is the fp16 X that the TMA put in ring slot s (landed before the
+        // converters could finish; the wait is for this thread's own view)
+        if (XH && !mbar_wait(fullA(s), (uint32_t)(i / SA) & 1u, abort_flag, &s_err_w8)) break;
         tc_fence_after();
-        const uint64_t db = smem_desc_sw128(base + P.xf_off + sc * SH::XF_SLOT);
+        const uint64_t db = smem_desc_sw128(XH ? base + s * SH::SLOT + SH::W_BYTES : base + P.xf_off + sc * SH::XF_SLOT);
         const uint32_t ta = tmem + SH::A_COL + SH::A_COLS * sc;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -587,6 +618,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
             tc_mma_f16_ta(tmem, ta + 8u * (4 * u + k), db + (uint64_t)((u * SH::XF_UNIT) >> 4) + (uint64_t)(2 * k),
                           idesc, (i > 0 || u > 0 || k > 0) ? 1u : 0u);
         tc_commit(emptyC(sc));
+        if (XH) tc_commit(emptyA(s));
       }
       // completes once every MMA issued above has finished (also on abort)
       tc_commit(bar_acc);
@@ -620,7 +652,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
       const uint32_t xin = st + SH::W_BYTES + xr * 128;
       const uint32_t xout = base + P.xf_off + sc * SH::XF_SLOT + xr * 128;
 #pragma unroll
-      for (int c2 = 0; c2 < SH::CPT; ++c2) {
+      for (int c2 = 0; c2 < (XH ? 0 : SH::CPT); ++c2) {
         const int c = part * SH::CPT + c2;
         const uint4 v = lds128(xin + ((c ^ (xr & 7)) << 4));
         const uint32_t w0 = v.x ^ 0x80808080u, w1 = v.y ^ 0x80808080u, w2 = v.z ^ 0x80808080u,
@@ -634,11 +666,11 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
       }
       tc_wait_st();
       tc_fence_before();
-      fence_proxy_async_smem();  // the fp16 X tile is read by the tensor core (async proxy)
+      if (!XH) fence_proxy_async_smem();  // the fp16 X tile is read by the tensor core (async proxy)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(fullC(sc));
-        mbar_arrive(emptyA(s));
+        if (!XH) mbar_arrive(emptyA(s));
       }
     }
   }
@@ -721,10 +753,10 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
   }
 }
 
-template <int BT>
+template <int BT, bool XH>
 tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8TcParams& P, dim3 grid, int S,
                         uint32_t smem, cudaStream_t stream) {
-  auto kern = w8tc_kernel<BT>;
+  auto kern = w8tc_kernel<BT, XH>;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW8SmemMax) != cudaSuccess)
@@ -754,16 +786,17 @@ tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8
 }
 
 // Shared memory of the tensor-memory kernel: ring, converted X slots, barriers, alignment slack.
-template <int BT>
+template <int BT, bool XH>
 uint32_t w8tc_smem(int stages) {
-  using SH = W8TcShape<BT>;
-  return stages * SH::SLOT + kW8TcConv * SH::XF_SLOT + 16 * stages + 16 * kW8TcConv + 16 + 1024;
+  using SH = W8TcShape<BT, XH>;
+  return stages * SH::SLOT + SH::CONV_SLOTS * SH::XF_SLOT + 16 * stages + 16 * kW8TcConv + 16 + 1024;
 }
 
-template <int BT>
-tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
+// xq: int8 codes, or (XH) the same codes as fp16 integers.
+template <int BT, bool XH>
+tm_status w8tc_run(const void* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
                    cudaStream_t stream) {
-  using SH = W8TcShape<BT>;
+  using SH = W8TcShape<BT, XH>;
   const int NB = (p->NT + 7) / 8, MB = (M + BT - 1) / BT;
   const int sms = num_sms(p->device);
   int S = split_k;
@@ -774,18 +807,19 @@ tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, voi
     while (S < 8 && (long long)NB * MB * S * 2 <= sms && p->KB / (2 * S) >= 2) S *= 2;
   }
   int stages = 8;
-  while (stages > 2 && w8tc_smem<BT>(stages) > kW8SmemMax) --stages;
-  const uint32_t smem = w8tc_smem<BT>(stages);
+  while (stages > 2 && w8tc_smem<BT, XH>(stages) > kW8SmemMax) --stages;
+  const uint32_t smem = w8tc_smem<BT, XH>(stages);
   if (smem > kW8SmemMax) return TM_ERR_UNSUPPORTED;
   CUtensorMap tmX;
   {
     EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return TM_ERR_CUDA;
     cuuint64_t dims[2] = {(cuuint64_t)p->K, (cuuint64_t)M};
-    cuuint64_t strides[1] = {(cuuint64_t)p->K};
-    cuuint32_t box[2] = {128, (cuuint32_t)BT};
+    cuuint64_t strides[1] = {(cuuint64_t)p->K * (XH ? 2 : 1)};
+    cuuint32_t box[2] = {XH ? 64u : 128u, (cuuint32_t)BT};  // 128 bytes per row either way
     cuuint32_t es[2] = {1, 1};
-    if (fn(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(xq), dims, strides, box, es,
+    if (fn(&tmX, XH ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(xq), dims,
+           strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TM_ERR_CUDA;
@@ -800,8 +834,9 @@ tm_status w8tc_run(const int8_t* xq, const float* sx, const tm_w8_packed* p, voi
   P.kb_per_cta = (p->KB + S - 1) / S;
   P.stages = stages;
   P.xf_off = stages * SH::SLOT;
-  P.bar_off = P.xf_off + kW8TcConv * SH::XF_SLOT;
-  return w8tc_launch_t<BT>(tmX, p->tm_codes, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem, stream);
+  P.bar_off = P.xf_off + SH::CONV_SLOTS * SH::XF_SLOT;
+  return w8tc_launch_t<BT, XH>(tmX, p->tm_codes, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem,
+                               stream);
 }
 
 int w8_mt(int M) { return M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8; }
@@ -912,10 +947,52 @@ extern "C" tm_status tm_w8a8_quantize_act(const uint16_t* X, int M, int K, int8_
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, w8_quant_act_kernel, reinterpret_cast<const __half*>(X), K, xq, sx) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, w8_quant_act_kernel<false>, reinterpret_cast<const __half*>(X), K, (void*)xq, sx) !=
+      cudaSuccess)
     return TM_ERR_CUDA;
   set_launch_count(1);
   return TM_OK;
+}
+
+extern "C" tm_status tm_w8a8_quantize_act_f16(const uint16_t* X, int M, int K, uint16_t* xq16, float* sx,
+                                              void* stream) {
+  if (!X || !xq16 || !sx || M < 0 || K <= 0 || K % 16) return TM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(X) & 15u) || (reinterpret_cast<uintptr_t>(xq16) & 15u) ||
+      (reinterpret_cast<uintptr_t>(sx) & 3u))
+    return TM_ERR_ALIGNMENT;
+  if (M == 0) return TM_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, w8_quant_act_kernel<true>, reinterpret_cast<const __half*>(X), K, (void*)xq16, sx) !=
+      cudaSuccess)
+    return TM_ERR_CUDA;
+  set_launch_count(1);
+  return TM_OK;
+}
+
+extern "C" tm_status tm_w8a8_gemm_f16(const uint16_t* xq16, const float* sx, const tm_w8_packed* p, void* Y, int M,
+                                      int split_k, int tile_m, void* stream) {
+  if (!xq16 || !sx || !p || !Y || M < 0) return TM_ERR_INVALID_ARG;
+  if (split_k < 0 || split_k > 8 || (split_k & (split_k - 1))) return TM_ERR_INVALID_ARG;
+  if (tile_m != 0 && tile_m != 64 && tile_m != 128 && tile_m != 256) return TM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(xq16) & 15u) || (reinterpret_cast<uintptr_t>(Y) & 15u) ||
+      (reinterpret_cast<uintptr_t>(sx) & 3u))
+    return TM_ERR_ALIGNMENT;
+  if (M == 0) return TM_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int BT = tile_m ? tile_m : w8tc_rows(M, p->NT, num_sms(p->device));
+  const tm_status r = BT == 64    ? w8tc_run<64, true>(xq16, sx, p, Y, M, split_k, st)
+                      : BT == 128 ? w8tc_run<128, true>(xq16, sx, p, Y, M, split_k, st)
+                                  : w8tc_run<256, true>(xq16, sx, p, Y, M, split_k, st);
+  if (r == TM_OK) set_launch_count(1);
+  return r;
 }
 
 extern "C" tm_status tm_w8_quantize_weight(const uint16_t* W, int K, int N, int8_t* q, float* sw, void* stream) {
@@ -1022,9 +1099,9 @@ extern "C" tm_status tm_w8a8_gemm_ex(const int8_t* xq, const float* sx, const tm
   if (M > 32) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int BT = tile_m ? tile_m : w8tc_rows(M, p->NT, num_sms(p->device));
-    const tm_status r = BT == 64    ? w8tc_run<64>(xq, sx, p, Y, M, split_k, st)
-                        : BT == 128 ? w8tc_run<128>(xq, sx, p, Y, M, split_k, st)
-                                    : w8tc_run<256>(xq, sx, p, Y, M, split_k, st);
+    const tm_status r = BT == 64    ? w8tc_run<64, false>(xq, sx, p, Y, M, split_k, st)
+                        : BT == 128 ? w8tc_run<128, false>(xq, sx, p, Y, M, split_k, st)
+                                    : w8tc_run<256, false>(xq, sx, p, Y, M, split_k, st);
     if (r == TM_OK) set_launch_count(1);
     return r;
   }
