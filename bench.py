@@ -903,10 +903,10 @@ def run_w8a8(args, rank, world, local, prefill=False):
         for it in items:
             if codes == "int8":
                 binding.w8a8_quantize_act(it["X"], out=(it["xq"], it["sx"]), stream=st)
-                binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
+                binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=st)
             else:
                 binding.w8a8_quantize_act_f16(it["X"], out=(it["xq"], it["sx"]), stream=st)
-                binding.w8a8_gemm_f16(it["xq"], it["sx"], it["w"], out=it["Y"], stream=st)
+                binding.w8a8_gemm_f16(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=st)
 
     with torch.cuda.stream(stream):
         launch_all(stream)
@@ -973,7 +973,7 @@ def run_w8a8(args, rank, world, local, prefill=False):
         "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"w8a8{'_prefill' if prefill else ''}: qkv, o_proj, gate_up, down x M",
-                   "activation_codes": codes,
+                   "activation_codes": codes, "tile_m": args.w8_tile_m or "auto",
                    "launches_per_step": 2 * len(items), "bytes_per_step": step_bytes, "flops_per_step": step_flops,
                    "l2": f"each GEMM has its own packed weights ({weight_bytes / 1e6:.0f} MB per step > 129 MB L2)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
@@ -1054,6 +1054,8 @@ def main(argv=None):
                    default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--w8-tile-m", type=int, choices=[0, 64, 128, 256], default=0,
+                   help="W8A8 rows of X per CTA of the tensor-memory kernel (0: automatic)")
     p.add_argument("--w8-codes", choices=["auto", "int8", "f16"], default="auto",
                    help="W8A8 activation codes: int8 or fp16 integers (auto: fp16 for prefill, int8 for decode)")
     p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
