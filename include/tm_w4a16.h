@@ -17,6 +17,11 @@
  *
  * Conventions for every call:
  *   - Pointers named "device" must point to memory of the current CUDA device.
+ *   - Kernels wait on barriers for at most about one second.  A wait that
+ *     gives up (a GPU time-sliced away for longer, or a copy that never
+ *     lands) cannot change the status the launching call already returned:
+ *     it sets a sticky device bit instead, and the outputs of that launch are
+ *     undefined (possibly stale) until tm_device_error reports the bit clear.
  *   - fp16 values travel as their 16-bit patterns (uint16_t) or as void*.
  *   - Nothing throws; every call returns a tm_status (or nothing).
  *   - Shapes: g in {64, 128}; K > 0 and K % g == 0; N > 0 and N % 16 == 0;

@@ -85,7 +85,9 @@ void tm_w8_packed_free(tm_w8_packed* p);
  * output columns x 64 or 128 rows, both operands converted to exact fp16 in
  * the kernel (weights into tensor memory, X into shared memory).
  * Waits are bounded: a copy that never lands sets the device timeout bit
- * (tm_device_error).
+ * (tm_device_error), and Y is then undefined (possibly stale) until
+ * tm_device_error reports the bit clear -- the status this call returned
+ * describes the launch only.
  */
 tm_status tm_w8a8_gemm(const int8_t* xq, const float* sx, const tm_w8_packed* p, void* Y, int M, int split_k,
                        void* stream);
@@ -113,6 +115,8 @@ tm_status tm_w8a8_quantize_act_f16(const uint16_t* X, int M, int K, uint16_t* xq
  * Every M runs the tensor-memory kernel (use tm_w8a8_gemm with int8 codes for
  * decode, M <= 32).  split_k and tile_m as in tm_w8a8_gemm_ex; for M > 32 the
  * result equals tm_w8a8_gemm_ex's bit for bit (same products, same order).
+ * Bounded waits as in tm_w8a8_gemm: after a timeout Y is undefined until
+ * tm_device_error reports the bit clear.
  *   xq16: device fp16 [M][K], 16-byte aligned;  sx: fp32 [M];  Y: fp16 [M][N], 16-byte aligned
  */
 tm_status tm_w8a8_gemm_f16(const uint16_t* xq16, const float* sx, const tm_w8_packed* p, void* Y, int M,

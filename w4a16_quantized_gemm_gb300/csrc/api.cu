@@ -64,6 +64,11 @@ void sm_shared_memory(int device, int* per_sm, int* reserved_per_cta) {
 
 void set_launch_count(int n) { t_launches = n; }
 
+int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess ? d : 0;
+}
+
 // Largest M the decode kernel serves, and the largest it gets when the path
 // is automatic; above that the tensor-memory kernel runs (measured faster on
 // GB300 from M = 33 up).

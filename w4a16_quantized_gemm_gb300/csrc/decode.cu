@@ -530,12 +530,8 @@ uint32_t residency_budget(int device, int ctas) {
 template <int MT, int WN, int NW, int UPS, bool XP>
 tm_status launch_t(const CUtensorMap& tmX, const DecodeParams& P, int S, uint32_t smem, cudaStream_t stream) {
   auto kern = decode_kernel<MT, WN, NW, UPS, XP>;
-  static bool attr_done = false;  // per instantiation, per process
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemPerCta) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation, one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)kSmemPerCta)) return TM_ERR_CUDA;
   constexpr int CN = NW * WN;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((P.NT + CN - 1) / CN), (unsigned)S, 1);

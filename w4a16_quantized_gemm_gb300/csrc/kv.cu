@@ -672,13 +672,8 @@ __global__ void __launch_bounds__(128) kv_append_kernel(const __half* __restrict
 template <int BITS, int G>
 tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
   constexpr uint32_t smem = KvSlot<BITS>::kSmem;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kv_attn_tc_kernel<BITS, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};  // one bit per device
+  if (!smem_attr_once(attr_set, (const void*)kv_attn_tc_kernel<BITS, G>, (int)smem)) return TM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * P.Hkv), (unsigned)S, 1);
   cfg.blockDim = dim3(kAttnThreads, 1, 1);
@@ -767,7 +762,7 @@ extern "C" tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc
     // split the tokens while the grid still fits in one wave of resident CTAs
     // and every CTA keeps at least four slots of tokens
     const uint32_t smem = bits == 8 ? KvSlot<8>::kSmem : KvSlot<4>::kSmem;
-    const long long slots = (long long)num_sms(0) * attn_resident(smem);
+    const long long slots = (long long)num_sms(current_device()) * attn_resident(smem);
     S = 1;
     while (S < kMaxSplit && (long long)B * Hkv * S * 2 <= slots && L / (2 * S) >= 4 * 16 * kSlotTiles) S *= 2;
   }

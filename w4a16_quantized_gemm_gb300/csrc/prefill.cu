@@ -349,12 +349,8 @@ template <int BN, int SA, int SB>
 tm_status launch_t(const CUtensorMap& tmX, const tm_packed* p, const PrefillParams& P, int S, cudaStream_t stream) {
   using SH = PrefillShape<BN, SA, SB>;
   auto kern = prefill_kernel<BN, SA, SB>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)SH::SMEM)) return TM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((P.NT + SH::NTB - 1) / SH::NTB), (unsigned)((P.M + kBM - 1) / kBM), (unsigned)S);
   cfg.blockDim = dim3(kPrefillThreads, 1, 1);

@@ -345,12 +345,8 @@ template <int G>
 tm_status rtn_tma_launch(const uint16_t* W, int K, int N, uint8_t* q, uint8_t* z, uint16_t* s, cudaStream_t st) {
   using SH = RtnTmaShape<G>;
   auto kern = rtn_tma_kernel<G>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SH::SMEM) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)SH::SMEM)) return TM_ERR_CUDA;
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return TM_ERR_CUDA;
   CUtensorMap tm;

@@ -455,12 +455,8 @@ template <int BT, int KU, int SB>
 tm_status tc_launch_t(const CUtensorMap& tmX, const tm_packed* p, const TcParams& P, int S, uint32_t smem,
                       cudaStream_t stream) {
   auto kern = tc_kernel<BT, KU, SB>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmemMax) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)kTcSmemMax)) return TM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((P.NT + kTcTiles - 1) / kTcTiles), (unsigned)((P.M + BT - 1) / BT), (unsigned)S);
   cfg.blockDim = dim3(kTcThreads, 1, 1);

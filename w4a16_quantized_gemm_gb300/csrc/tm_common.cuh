@@ -3,6 +3,8 @@
 // on sm_103a.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -115,6 +117,21 @@ int num_sms(int device);
 // system reserves for each CTA (bytes).
 void sm_shared_memory(int device, int* per_sm, int* reserved_per_cta);
 void set_launch_count(int n);
+// The device current on this thread (0 when the query fails).
+int current_device();
+
+// The dynamic shared-memory limit of a kernel is a per-device setting: raise
+// it once per (kernel, device).  `done` is the kernel's own flag word (bit d =
+// device d); two threads making their first call at once may both set it,
+// which is harmless.
+inline bool smem_attr_once(std::atomic<unsigned long long>& done, const void* kern, int bytes) {
+  const int dev = current_device();
+  const unsigned long long bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
+}
 
 // Decode / prefill launchers (decode.cu, prefill.cu).
 tm_status plan_decode(const tm_packed* p, int M, const tm_gemm_config* in, tm_gemm_config* out);

@@ -757,12 +757,8 @@ template <int BT, bool XH>
 tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8TcParams& P, dim3 grid, int S,
                         uint32_t smem, cudaStream_t stream) {
   auto kern = w8tc_kernel<BT, XH>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW8SmemMax) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)kW8SmemMax)) return TM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kW8TcThreads, 1, 1);
@@ -884,12 +880,8 @@ template <int MT>
 tm_status w8_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8Params& P, dim3 grid, int S,
                       uint32_t smem, cudaStream_t stream) {
   auto kern = w8_kernel<MT>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kW8SmemMax) != cudaSuccess)
-      return TM_ERR_CUDA;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // one bit per device
+  if (!smem_attr_once(attr_done, (const void*)kern, (int)kW8SmemMax)) return TM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3((kW8NW + 1) * 32, 1, 1);
