@@ -44,7 +44,8 @@ typedef enum {
   TM_ERR_UNSUPPORTED = 3,   /* valid request this build does not serve (e.g. no sm_103a device) */
   TM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
   TM_ERR_DEVICE_TIMEOUT = 5,/* a kernel gave up waiting on a barrier (reported by tm_device_error) */
-  TM_ERR_BAD_CODE = 6       /* a code or zero above 15 was passed to tm_pack_weights */
+  TM_ERR_BAD_CODE = 6,      /* a code or zero above 15 was passed to tm_pack_weights */
+  TM_ERR_SCRATCH_LIMIT = 7  /* the request does not fit the static staging array of tm_w4a16_gemm_host_static */
 } tm_status;
 
 /* Opaque packed weights.  Owns one device allocation (codes, scales, zeros in
@@ -252,6 +253,47 @@ tm_status tm_w4a16_gemm_host(const void* X_host, const tm_packed* p, void* Y_hos
  */
 tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, const int* M, const void* X_host, void* Y_host,
                                    void* X_dev, void* Y_dev, void* stream);
+
+/*
+ * Bytes of the device array behind tm_w4a16_gemm_host_static.  Every device
+ * on which the library is loaded reserves this much memory when the module
+ * loads there, and keeps it until the process exits.
+ */
+#define TM_STATIC_STAGING_BYTES (8u << 20)
+
+/*
+ * tm_w4a16_gemm_host without caller-provided device buffers, for callers
+ * that cannot allocate device memory when they need the product: a plug-in
+ * whose host application has already reserved the device for its own memory
+ * pool (cudaMalloc then fails, or eats into that pool), or a latency-critical
+ * loop where cudaMalloc / cudaFree may block or synchronise the device.  The
+ * paper has no counterpart to this call; it is a property of this library.
+ *
+ * X_host (fp16 [M][K]) is copied into a fixed __device__ array of
+ * TM_STATIC_STAGING_BYTES bytes, the product runs as tm_w4a16_gemm_ex from
+ * there into the same array (Y at the first 256-byte boundary after X), and
+ * Y comes back into Y_host (fp16 [M][N]).  Asynchronous on `stream`; the
+ * caller synchronises the stream before reading Y_host.  Pinned host memory
+ * lets the copies run asynchronously; pageable memory makes them block.
+ *
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.
+ *
+ * Every call on a device shares the one array, which keeps the last call's
+ * contents (nothing in it has to start at zero: X is copied in whole and Y
+ * written in whole).  Calls whose copies or kernels overlap on the GPU --
+ * on different streams, or from different host threads without ordering --
+ * race on it and corrupt each other's X and Y: issue them on one stream.
+ *
+ * Errors: TM_ERR_INVALID_ARG for NULL pointers, M < 0, or a handle packed on
+ * another device than the current one; TM_ERR_SCRATCH_LIMIT when
+ * round_up(2 M K, 256) + 2 M N exceeds TM_STATIC_STAGING_BYTES (nothing is
+ * copied or launched); otherwise as tm_w4a16_gemm_host.  M == 0 is a no-op.
+ */
+tm_status tm_w4a16_gemm_host_static(const void* X_host, const tm_packed* p, void* Y_host, int M,
+                                    const tm_gemm_config* cfg, void* stream);
 
 /* The settings tm_w4a16_gemm would use for this handle and M (all fields filled in). */
 tm_status tm_gemm_plan(const tm_packed* p, int M, const tm_gemm_config* cfg, tm_gemm_config* out);

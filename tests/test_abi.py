@@ -55,7 +55,7 @@ def test_binding_names_match_header():
 
 def test_status_strings(lib):
     from w4a16_quantized_gemm_gb300 import binding
-    for st in range(7):
+    for st in range(8):
         assert binding.status_str(st) == binding._STATUS[st]
     assert binding.status_str(99) == "unknown status"
 

@@ -17,7 +17,8 @@ from . import build as _build
 
 TM_OK = 0
 _STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not 16-byte aligned", 3: "unsupported configuration",
-           4: "CUDA call failed", 5: "device barrier timeout", 6: "code or zero above 15"}
+           4: "CUDA call failed", 5: "device barrier timeout", 6: "code or zero above 15",
+           7: "request exceeds the static staging array"}
 
 EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_weights", "tm_packed_info",
            "tm_packed_free", "tm_w4a16_gemm", "tm_w4a16_gemm_ex", "tm_gemm_plan", "tm_device_error",
@@ -25,7 +26,7 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
            "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
            "tm_w8_quantize_weight", "tm_kv_append", "tm_w4a16_gemm_host", "tm_w4a16_gemm_host_batch",
-           "tm_w8a8_quantize_act_f16", "tm_w8a8_gemm_f16")
+           "tm_w8a8_quantize_act_f16", "tm_w8a8_gemm_f16", "tm_w4a16_gemm_host_static")
 
 
 class TMError(RuntimeError):
@@ -79,6 +80,8 @@ def load(path: Optional[str] = None):
     lib.tm_w4a16_gemm_ex.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
     lib.tm_w4a16_gemm_host.restype = ci
     lib.tm_w4a16_gemm_host.argtypes = [vp, vp, vp, ci, vp, vp, ctypes.POINTER(GemmConfig), vp]
+    lib.tm_w4a16_gemm_host_static.restype = ci
+    lib.tm_w4a16_gemm_host_static.argtypes = [vp, vp, vp, ci, ctypes.POINTER(GemmConfig), vp]
     lib.tm_w4a16_gemm_host_batch.restype = ci
     lib.tm_w4a16_gemm_host_batch.argtypes = [ci, ctypes.POINTER(vp), ctypes.POINTER(ci), vp, vp, vp, vp, vp]
     lib.tm_gemm_plan.restype = ci
@@ -308,6 +311,33 @@ def gemm_host(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = N
     _check(load().tm_w4a16_gemm_host(X.data_ptr(), w.handle, out.data_ptr(), M, X_dev.data_ptr(), Y_dev.data_ptr(),
                                      ctypes.byref(c) if c else None, ctypes.c_void_p(s.cuda_stream)),
            "tm_w4a16_gemm_host")
+    if sync:
+        s.synchronize()
+    return out
+
+
+STATIC_STAGING_BYTES = 8 << 20  # TM_STATIC_STAGING_BYTES
+
+
+def gemm_host_static(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor] = None, config=None,
+                     stream: Optional[torch.cuda.Stream] = None, sync: bool = True) -> torch.Tensor:
+    """tm_w4a16_gemm_host_static: as ``gemm_host``, but staged through the
+    library's fixed device array, so that the call allocates no device memory
+    (``out``, the host result, is allocated here when None).  Calls share the
+    array: issue them on one stream."""
+    if X.dim() != 2:
+        raise ValueError("X must be fp16 [M][K]")
+    M = X.shape[0]
+    _host_fp16(X, (M, w.K), "X")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.float16, pin_memory=True)
+    _host_fp16(out, (M, w.N), "out")
+    s = stream if stream is not None else torch.cuda.current_stream(w.device)
+    c = _cfg(config)
+    with torch.cuda.device(w.device):
+        _check(load().tm_w4a16_gemm_host_static(X.data_ptr(), w.handle, out.data_ptr(), M,
+                                                ctypes.byref(c) if c else None, ctypes.c_void_p(s.cuda_stream)),
+               "tm_w4a16_gemm_host_static")
     if sync:
         s.synchronize()
     return out

@@ -129,6 +129,7 @@ extern "C" const char* tm_status_str(tm_status s) {
     case TM_ERR_CUDA: return "CUDA call failed";
     case TM_ERR_DEVICE_TIMEOUT: return "device barrier timeout";
     case TM_ERR_BAD_CODE: return "code or zero above 15";
+    case TM_ERR_SCRATCH_LIMIT: return "request exceeds the static staging array";
   }
   return "unknown status";
 }
