@@ -16,9 +16,17 @@ from HBM).  A step is captured once as a CUDA graph and replayed.
   cpu_baseline = the fp64 oracle on a bounded column sample of the same
               workload, extrapolated to the full step, on the host cores.
 
+  detail    = every configuration of the metric (workloads 0-4: the 1x4096x4096
+              GEMM, the 8B decode and prefill shapes, the 70B shapes, the
+              group-size/outlier stress shapes), each GEMM in steady state
+              with its own roofline; the 8B layer linears per M and for
+              M <= 16 together; the prefill step (TFLOP/s against the burst
+              tensor peak).  --no-detail skips it.
+
 --workload prefill runs the Llama-3-8B prefill shapes (M in {128,1024,4096},
 TFLOP/s of the tensor-memory kernel against the measured tensor peak) instead.
---impl reference times the oracle as the reference arm.
+--impl reference times the oracle as the reference arm: the whole workload per
+step when the run fits its time budget, else a labelled column sample.
 """
 from __future__ import annotations
 
@@ -76,6 +84,30 @@ def w8a8_bytes(M, K, N):
     """One W8A8 layer: the quantiser reads fp16 X and writes int8 X and s_x; the
     GEMM reads the int8 weights, their fp32 scales, int8 X and s_x, writes fp16 Y."""
     return (2 * M * K + M * K + 4 * M) + (K * N + 4 * N + M * K + 4 * M + 2 * M * N)
+
+
+def workload_config(kind, world=1):
+    """The `config` object both arms print: the workload and its sizes only."""
+    from w4a16_quantized_gemm_gb300 import synth
+    cases = synth.workload(WORKLOADS[kind]["idx"])
+    return {"workload": WORKLOADS[kind]["name"], "gemms_per_step": len(cases),
+            "bytes_per_step": sum(algorithmic_bytes(c.M, c.K, c.N, c.g) for c in cases),
+            "flops_per_step": sum(flops(c.M, c.K, c.N) for c in cases),
+            "l2": "inputs larger than L2: every GEMM of a step has its own weights (>129 MB per step)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def roofline_entry(nbytes, nflops, seconds, peaks, tensor_peak="bf16_tflops"):
+    """Roofline of one timed unit: the bound is whichever of bytes / HBM and
+    flops / tensor peak takes longer; achieved is that quantity per second."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = nflops / (peaks[tensor_peak] * 1e12)
+    if t_hbm >= t_tc:
+        ach, peak, unit, bound = nbytes / seconds / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+    else:
+        ach, peak, unit, bound = nflops / seconds / 1e12, peaks[tensor_peak], "TFLOP/s", "tensor"
+    return {"bound": bound, "achieved": round(ach, 1), "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
+            "peak_source": peaks["source"] + (" (sustained)" if tensor_peak.endswith("sustained") else "")}
 
 
 def load_peaks():
@@ -309,11 +341,10 @@ def run_gpu(args, rank, world, local):
 
     t_max_s = reduce_max(t_total_ms / 1e3, world)
 
-    # Per-GEMM steady-state detail (not the headline): each GEMM launched back
-    # to back on enough distinct copies of its packed weights to exceed L2,
-    # captured as one graph; time per launch = replay time / copies.
-    detail = per_gemm_detail(wl, stream, peaks) if args.detail else []
     step_s = statistics.mean(step_ms) * 1e-3
+    # Every configuration of the metric, each GEMM in steady state and the
+    # step-level figures (not the headline value; see config_detail).
+    detail = [] if args.no_detail else config_detail(wl, stream, peaks, args)
 
     if spec["unit"] == "GB/s":
         per_rank_units = wl.step_bytes * args.steps / 1e9
@@ -324,7 +355,7 @@ def run_gpu(args, rank, world, local):
     else:
         per_rank_units = wl.step_flops * args.steps / 1e12
         achieved = wl.step_flops / step_s / 1e12
-        peak = peaks["bf16_tflops_sustained"]
+        peak = peaks["bf16_tflops"]  # a ms-scale step: the burst peak
         traffic = read_traffic("tc", "llama3_8b_prefill")
         unit_kernel = "TFLOP/s"
     value = aggregate(per_rank_units, world, t_max_s)
@@ -336,12 +367,9 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": round(value, 2), "unit": spec["unit"], "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": spec["name"], "gemms_per_step": len(wl.items),
-                   "bytes_per_step": wl.step_bytes, "flops_per_step": wl.step_flops,
-                   "packed_weight_bytes_per_step": wl.weight_bytes,
-                   "accumulate": "f32", "launch": f"one CUDA graph per step ({len(wl.items)} kernel nodes)",
-                   "l2": "inputs larger than L2: every GEMM of a step has its own weights (>129 MB per step)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(args.workload, world),
+        "launch": f"one CUDA graph per step ({len(wl.items)} kernel nodes, programmatic dependent launch); "
+                  f"{wl.weight_bytes} bytes of distinct packed weights per step; fp32 accumulation",
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
                      "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peaks["source"],
@@ -360,42 +388,136 @@ def run_gpu(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
-def per_gemm_detail(wl, stream, peaks, min_bytes=300e6, reps=5):
+def _time_graph(launch, stream, reps):
+    """Capture ``launch(stream)`` as one CUDA graph, replay it once untimed,
+    then ``reps`` times between CUDA events on ``stream``: ms per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        launch(stream)  # outside capture: attributes, module load
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        launch(torch.cuda.current_stream())
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    del g
+    return ms
+
+
+def _pack_copies(key, device, min_bytes):
+    """Distinct packed copies of one synthetic weight (q, z, s of the case's
+    recipe) until together they exceed ``min_bytes`` (> L2)."""
+    import numpy as np
     import torch
 
+    from w4a16_quantized_gemm_gb300 import binding, synth
+    K, N, g, stress = key
+    q, z, s, sal = synth.weights(K, N, g, stress)
+    qd = torch.from_numpy(q).to(device)
+    zd = torch.from_numpy(z).to(device)
+    sd = torch.from_numpy(s.view(np.uint16)).to(device).view(torch.float16)
+    copies = [binding.pack(qd, zd, sd, g)]
+    while len(copies) * copies[0].nbytes < min_bytes:
+        copies.append(binding.pack(qd, zd, sd, g))
+    del qd, zd, sd
+    return copies, sal
+
+
+def _decode_step_at_m(wl, M, stream, peaks, rounds=3):
+    """The four Llama-3-8B layers of the headline workload at one M (qkv,
+    o_proj, gate_up, down: one decoder layer's linears at batch M), launched in
+    order on `rounds` distinct copies of their weights (> L2 together)."""
     from w4a16_quantized_gemm_gb300 import binding
-    out = []
-    for it in wl.items:
-        c = it["case"]
-        copies = [it["w"]]
-        q, z, s = it["w"].unpack()
-        while len(copies) * it["w"].nbytes < min_bytes:
-            copies.append(binding.pack(q, z, s, c.g))
-        del q, z, s
-        with torch.cuda.stream(stream):
-            for w in copies:
-                binding.gemm(it["X"], w, out=it["Y"], stream=stream)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for w in copies:
-                binding.gemm(it["X"], w, out=it["Y"], stream=torch.cuda.current_stream())
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        stream.synchronize()
-        ms = e0.elapsed_time(e1) / (reps * len(copies))
-        del g
-        for w in copies[1:]:
+    items = [it for it in wl.items if it["case"].M == M]
+    sets = [[it["w"] for it in items]]
+    for _ in range(rounds - 1):
+        sets.append([])
+        for it in items:
+            q, z, s_ = it["w"].unpack()
+            sets[-1].append(binding.pack(q, z, s_, it["case"].g))
+            del q, z, s_
+
+    def launch(st):
+        for ws in sets:
+            for it, w in zip(items, ws):
+                binding.gemm(it["X"], w, out=it["Y"], stream=st)
+    ms = _time_graph(launch, stream, 10) / rounds
+    for ws in sets[1:]:
+        for w in ws:
             w.free()
-        rt = max(it["bytes"] / (peaks["hbm_gbs"] * 1e9), it["flops"] / (peaks["bf16_tflops"] * 1e12))
-        out.append({"gemm": c.name, "us": round(ms * 1e3, 2), "GB/s": round(it["bytes"] / (ms * 1e-3) / 1e9, 1),
-                    "TFLOP/s": round(it["flops"] / (ms * 1e-3) / 1e12, 1),
-                    "roofline_frac": round(rt / (ms * 1e-3), 3), "plan": it["plan"]})
+    nbytes = sum(it["bytes"] for it in items)
+    nflops = sum(it["flops"] for it in items)
+    return {"config": 1, "step": f"llama3-8b layer linears at M={M}", "M": M, "us": round(ms * 1e3, 2),
+            "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes,
+            "roofline": roofline_entry(nbytes, nflops, ms * 1e-3, peaks)}
+
+
+def _prefill_step(device, stream, peaks, steps):
+    """Workload 2 as one step (the 12 prefill GEMMs, each with its own weights)
+    captured as a graph: TFLOP/s against the burst tensor peak."""
+    wl = Workload("prefill", device)
+    ms = _time_graph(lambda st: wl.launch_all(st), stream, steps)
+    for it in wl.items:
+        it["w"].free()
+    return {"config": 2, "step": WORKLOADS["prefill"]["name"], "us": round(ms * 1e3, 1),
+            "TFLOP/s": round(wl.step_flops / (ms * 1e-3) / 1e12, 1), "flops": wl.step_flops,
+            "roofline": roofline_entry(wl.step_bytes, wl.step_flops, ms * 1e-3, peaks)}
+
+
+def config_detail(wl, stream, peaks, args, min_bytes=300e6, reps=5):
+    """Every configuration of the metric (workloads 0-4), each GEMM in steady
+    state: launched back to back (programmatic dependent launch) on enough
+    distinct copies of its packed weights to exceed L2, captured as one graph;
+    time per launch = replay time / copies, with its own roofline (burst
+    tensor peak: every replay lasts milliseconds at most).  Then the step-level
+    figures: the headline workload's layer linears per M (and M <= 16
+    together), and the prefill step of workload 2."""
+    import numpy as np
+    import torch
+
+    from w4a16_quantized_gemm_gb300 import binding, synth
+    device = wl.items[0]["X"].device
+    out = []
+    groups = {}
+    for ci in range(5):
+        for c in synth.workload(ci):
+            groups.setdefault((c.K, c.N, c.g, c.stress), []).append((ci, c))
+    for key, cases in groups.items():
+        copies, sal = _pack_copies(key, device, min_bytes)
+        for ci, c in cases:
+            Xh = synth.activations(c.M, c.K, sal, 0, tag=f"/N{c.N}/g{c.g}" + ("/stress" if c.stress else ""))
+            X = torch.from_numpy(Xh.view(np.uint16)).to(device).view(torch.float16)
+            Y = torch.empty((c.M, c.N), dtype=torch.float16, device=device)
+
+            def launch(st, X=X, Y=Y):
+                for w in copies:
+                    binding.gemm(X, w, out=Y, stream=st)
+            ms = _time_graph(launch, stream, reps) / len(copies)
+            nb, nf = algorithmic_bytes(c.M, c.K, c.N, c.g), flops(c.M, c.K, c.N)
+            out.append({"config": ci, "gemm": c.name, "M": c.M, "us": round(ms * 1e3, 2),
+                        "GB/s": round(nb / (ms * 1e-3) / 1e9, 1), "TFLOP/s": round(nf / (ms * 1e-3) / 1e12, 1),
+                        "plan": binding.plan(copies[0], c.M), "roofline": roofline_entry(nb, nf, ms * 1e-3, peaks)})
+            del X, Y
+        for w in copies:
+            w.free()
+        del copies
+        torch.cuda.empty_cache()
+    steps = [_decode_step_at_m(wl, M, stream, peaks) for M in (1, 8, 16, 32)]
+    out.extend(steps)
+    small = [e for e in steps if e["M"] <= 16]
+    nb = sum(e["bytes"] for e in small)
+    t = sum(e["us"] for e in small) * 1e-6
+    out.append({"config": 1, "step": "llama3-8b layer linears at M in {1,8,16} (the decode target's range)",
+                "us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
+                "roofline": roofline_entry(nb, 0, t, peaks)})
+    out.append(_prefill_step(device, stream, peaks, max(5, min(args.steps, 50))))
     return out
 
 
@@ -491,41 +613,67 @@ def cpu_baseline(wl, budget_s):
     return {"value": round(units / t_full, 4), "unit": spec["unit"], "cores": threads, "kind": "oracle",
             "sample": f"every GEMM of one step on its first {cols} output columns (all M rows, full K); "
                       f"{t_sample:.1f} s measured, scaled by N/{cols} per GEMM to a full step "
-                      f"({t_full:.1f} s)"}
+                      f"({t_full:.1f} s)",
+            "config0_one_thread": config0_one_thread()}
+
+
+def config0_one_thread():
+    """The oracle on workload 0 (one 1x4096x4096 GEMM, g = 128) in full, one
+    thread: the single-core baseline of the smallest configuration."""
+    import oracle
+    from w4a16_quantized_gemm_gb300 import synth
+    c = synth.workload(0)[0]
+    p = synth.case_problem(c)
+    oracle.gemm(p.X, p.q, p.z, p.s, c.g, threads=1)  # warm (page in, first call)
+    t0 = time.perf_counter()
+    oracle.gemm(p.X, p.q, p.z, p.s, c.g, threads=1)
+    dt = time.perf_counter() - t0
+    nb = algorithmic_bytes(c.M, c.K, c.N, c.g)
+    return {"gemm": c.name, "ms": round(dt * 1e3, 2), "GB/s": round(nb / dt / 1e9, 4), "cores": 1}
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the oracle as it stands, on the host cores."""
+    """The reference arm: the oracle as it stands, on the host cores.  Each
+    step is the whole workload when that fits the run's time budget (every
+    GEMM of the step in full); otherwise every GEMM on its first C output
+    columns, C chosen for the budget, and the line says so.  ms_per_step and
+    value are what was measured on the work that ran."""
     if rank != 0:
         return
     import oracle
-    from w4a16_quantized_gemm_gb300 import synth
     spec = WORKLOADS[args.workload]
     threads = oracle.default_threads()
     cw = _cases_with_weights(args.workload)
-    per_step = max(0.5, min(4.0, 120.0 / max(1, args.steps + args.warmup)))
-    cols = _calibrated_cols(cw, per_step, threads)
+    budget_s = 150.0  # the whole --steps/--warmup run
+    full_cols = max(c.N for (c, *_r) in cw)
+    t_probe, t_full_est = _oracle_sample(cw, 64, threads)
+    steps_total = args.steps + args.warmup
+    if t_full_est * steps_total <= budget_s:
+        cols = full_cols
+    else:
+        cols = max(16, int(full_cols * budget_s / (t_full_est * steps_total)) // 16 * 16)
     for _ in range(args.warmup):
         _oracle_sample(cw, cols, threads)
-    t_s = 0.0
-    t_full = 0.0
+    t_run = 0.0
     for _ in range(args.steps):
-        a, b = _oracle_sample(cw, cols, threads)
-        t_s += a
-        t_full += b
-    bytes_step = sum(algorithmic_bytes(c.M, c.K, c.N, c.g) for (c, *_r) in cw)
-    flops_step = sum(flops(c.M, c.K, c.N) for (c, *_r) in cw)
-    units = bytes_step / 1e9 if spec["unit"] == "GB/s" else flops_step / 1e12
-    value = units * args.steps / t_full
-    sample = (f"each step: every GEMM on its first {cols} output columns (all M rows, full K), "
-              f"scaled by N/{cols} per GEMM to a full step")
+        a, _b = _oracle_sample(cw, cols, threads)
+        t_run += a
+    done_bytes = sum(algorithmic_bytes(c.M, c.K, min(c.N, cols), c.g) for (c, *_r) in cw)
+    done_flops = sum(flops(c.M, c.K, min(c.N, cols)) for (c, *_r) in cw)
+    units = done_bytes / 1e9 if spec["unit"] == "GB/s" else done_flops / 1e12
+    value = units * args.steps / t_run
+    if cols >= full_cols:
+        sample = "every step the whole workload (every GEMM in full)"
+    else:
+        sample = (f"every step each GEMM on its first {cols} output columns (all M rows, full K): "
+                  f"{done_bytes} algorithmic bytes per step, value = those bytes / measured time")
+    cfg = workload_config(args.workload)
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": spec["unit"],
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-           "ms_per_step": round(t_full * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": spec["name"], "gemms_per_step": len(cw)},
+           "ms_per_step": round(t_run * 1e3 / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
            "cpu_baseline": {"value": round(value, 4), "unit": spec["unit"], "cores": threads, "kind": "oracle",
-                            "sample": sample},
+                            "sample": sample, "config0_one_thread": config0_one_thread()},
            "e2e": {"value": round(value, 4), "unit": spec["unit"], "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -1058,7 +1206,9 @@ def main(argv=None):
                    help="W8A8 rows of X per CTA of the tensor-memory kernel (0: automatic)")
     p.add_argument("--w8-codes", choices=["auto", "int8", "f16"], default="auto",
                    help="W8A8 activation codes: int8 or fp16 integers (auto: fp16 for prefill, int8 for decode)")
-    p.add_argument("--detail", action="store_true", help="also time every GEMM alone (steady state)")
+    p.add_argument("--no-detail", action="store_true",
+                   help="skip the per-configuration detail (every GEMM of workloads 0-4 in steady state, "
+                        "the per-M decode steps and the prefill step)")
     p.add_argument("--single", default=None, help="M,K,N,g: one GEMM 15 times, cold L2 (for ncu captures)")
     p.add_argument("--path", type=int, default=0,
                    help="with --single: 1 decode, 2 prefill (shared-memory W^T), 3 tensor-memory, 0 automatic")

@@ -23,6 +23,8 @@ linear layers):
 from __future__ import annotations
 
 import dataclasses
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Dict, List, Optional, Tuple
 
 import numpy as np
@@ -59,11 +61,27 @@ def draws(key: int, n: int, offset: int = 0) -> np.ndarray:
         return _mix(np.uint64(key) + i * _GAMMA)
 
 
+def _chunks(n: int, work) -> None:
+    """Run ``work(a, b)`` over [0, n) in chunks of _CHUNK, on a thread pool when
+    there is more than one chunk (NumPy releases the GIL inside its array
+    operations; each chunk writes its own slice, so the result does not depend
+    on the thread count)."""
+    spans = [(a, min(n, a + _CHUNK)) for a in range(0, n, _CHUNK)]
+    if len(spans) <= 1:
+        for a, b in spans:
+            work(a, b)
+        return
+    with ThreadPoolExecutor(max_workers=min(len(spans), os.cpu_count() or 1)) as ex:
+        list(ex.map(lambda ab: work(*ab), spans))
+
+
 def _fill(key: int, n: int, fn, dtype) -> np.ndarray:
     out = np.empty(n, dtype=dtype)
-    for a in range(0, n, _CHUNK):
-        b = min(n, a + _CHUNK)
+
+    def work(a, b):
         out[a:b] = fn(draws(key, b - a, a))
+
+    _chunks(n, work)
     return out
 
 
@@ -90,12 +108,14 @@ def normal64(tag: str, rows: int, cols: int) -> np.ndarray:
     n = rows * cols
     key = stream_key(tag)
     out = np.empty(n, dtype=np.float64)
-    for a in range(0, n, _CHUNK):
-        b = min(n, a + _CHUNK)
+
+    def work(a, b):
         r = draws(key, 2 * (b - a), 2 * a)
         u1 = ((r[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
         u2 = _unit(r[1::2])
         out[a:b] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+    _chunks(n, work)
     return out.reshape(rows, cols)
 
 
