@@ -13,8 +13,10 @@ directly.  Readings (ours, where the pages stop):
     oracle takes the kernel's precision):
         lo = min(0, min x), hi = max(0, max x); r = hi - lo, or B if r == 0
         s = fp16(r / B), at least 2^-24;  z = clamp(rint(-lo / s), 0, B)
-        i = 1 / s;  q = clamp(rint(x * i) + z, 0, B)
-    -- the same rule as the weight quantiser, along the head dimension;
+        q = clamp(rint(x / s) + z, 0, B)          (one division per value)
+    -- the same rule as the weight quantiser, along the head dimension (x and
+    s are fp16, so the binary32 quotient rounds to the same integer as the
+    exact one);
   * storage: codes [.., D] one byte each (int8) or two per byte, even index in
     the low nibble (int4); s fp16 and z uint8 per (token, head);
   * decode attention for one query token per sequence, grouped-query heads
@@ -46,8 +48,7 @@ def quantize(X: np.ndarray, bits: int):
     s16 = np.maximum((r / B).astype(np.float16), _TINY)
     sf = s16.astype(np.float32)
     z = np.clip(np.rint(-lo / sf), 0, B).astype(np.float32)
-    inv = np.float32(1) / sf
-    q = np.clip(np.rint(x * inv[..., None]) + z[..., None], 0, B).astype(np.uint8)
+    q = np.clip(np.rint(x / sf[..., None]) + z[..., None], 0, B).astype(np.uint8)  # binary32 division
     if bits == 4:
         q = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
     return q, s16, z.astype(np.uint8)

@@ -13,14 +13,17 @@ exact binary32 values:
     r  = hi - lo, or 15 when hi == lo (an all-zero group)
     s  = fp16(r / 15), at least the smallest positive fp16 (2^-24)
     z  = clamp(rint(-lo / s), 0, 15)
-    i  = 1 / s                                  (one reciprocal per group and column)
-    q  = clamp(rint(w * i) + z, 0, 15)
+    q  = clamp(rint(w / s) + z, 0, 15)          (one division per weight)
 
 Every operation is one IEEE binary32 operation with round-to-nearest-even
 (rint ties to even), in this order.  The pages leave the precision open and
-these values decide integers (codes), so the oracle takes the kernel's
-precision, binary32, rather than binary64: both sides then make the same
-decision on every tie.  Pinned by ``tests/test_oracle_rtn.py``.
+these values decide integers (codes), so the oracle states the precision in
+which each decision is taken.  For the code itself binary32 and exact
+arithmetic agree: w and s are fp16 values, and a quotient of two fp16 values
+that is not a half-integer lies at least 1/8188 away from every half-integer,
+far more than the binary32 rounding of the quotient can move it.  Pinned by
+``tests/test_oracle_rtn.py`` (including exact ties at scales whose reciprocal
+is inexact, where w * (1/s) would round the wrong way).
 """
 from __future__ import annotations
 
@@ -47,8 +50,7 @@ def quantize(W: np.ndarray, g: int):
     s16 = np.maximum(s16, _TINY)
     sf = s16.astype(np.float32)                                 # exact
     z = np.clip(np.rint(-lo / sf), 0, 15).astype(np.float32)
-    inv = np.float32(1) / sf
-    q = np.clip(np.rint(w * inv[:, None, :]) + z[:, None, :], 0, 15)
+    q = np.clip(np.rint(w / sf[:, None, :]) + z[:, None, :], 0, 15)  # binary32 division per weight
     return q.reshape(K, N).astype(np.uint8), z.astype(np.uint8), s16
 
 

@@ -12,11 +12,13 @@ preceding layer beforehand, so the GEMM never sees them):
 
   * activations, per token (row m of X [M][K]), symmetric and dynamic:
         a  = max_k |x|;  s_x = a / 127, or 1 when a == 0
-        i  = 1 / s_x;    q_x = clamp(rint(x * i), -127, 127)
+        q_x = clamp(rint(x / s_x), -127, 127)        (one division per value)
   * weights, per output channel (column n of W [K][N]), the same rule:
-        s_w = max_k |w| / 127 (or 1);  q_w = clamp(rint(w * (1 / s_w)), -127, 127)
+        s_w = max_k |w| / 127 (or 1);  q_w = clamp(rint(w / s_w), -127, 127)
   * every step one IEEE binary32 operation with round-to-nearest-even (the
-    decisions are integers, so the oracle takes the kernel's precision);
+    decisions are integers, so the oracle states their precision; s is a
+    binary32 value here, and x * (1 / s) can differ from x / s by enough to
+    move a code, e.g. at a = 0.50146484375, x = a / 2);
   * the product:  Y[m][n] = s_x[m] s_w[n] sum_k q_x[m][k] q_w[k][n]
     -- the integer sum exact (int64 here), the scaling in binary64.
 
@@ -36,8 +38,7 @@ def _quantize_rows(x: np.ndarray):
     a = np.abs(x).max(axis=1)
     s = a / np.float32(QMAX)                         # one binary32 division
     s = np.where(a == np.float32(0), np.float32(1), s).astype(np.float32)
-    inv = (np.float32(1) / s).astype(np.float32)
-    q = np.clip(np.rint(x * inv[:, None]), -QMAX, QMAX).astype(np.int8)
+    q = np.clip(np.rint(x / s[:, None]), -QMAX, QMAX).astype(np.int8)  # binary32 division per value
     return q, s
 
 

@@ -42,6 +42,16 @@ def pins(quantize, attention):
     c, s, z = quantize(X, 4)
     out["nibbles"] = bool(np.array_equal(c[0], [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE])
                           and float(s[0]) == 0.25 and z[0] == 0)
+    # int8 exact ties at a scale whose binary32 reciprocal is inexact: max
+    # 1.7431640625 = 255 * 0.0068359375 (= 255 * 7 * 2^-10) gives s = 0.0068359375
+    # (fp16 bits 0x1F00) exactly, z = 0; 6.5 s, 12.5 s, 14.5 s are fp16 values whose
+    # quotient by s is exactly the half-integer -> the even codes 6, 12, 14
+    # (x * fl(1/s) would give 7, 13, 15); 0.5, 1.0, 0.25 divide to 73.14, 146.29, 36.57.
+    X = np.array([[0.0, 1.7431640625, 0.04443359375, 0.08544921875, 0.09912109375, 0.5, 1.0, 0.25]],
+                 dtype=np.float16)
+    c, s, z = quantize(X, 8)
+    out["ties_inexact_reciprocal"] = bool(s.view(np.uint16)[0] == 0x1F00 and z[0] == 0
+                                          and np.array_equal(c[0], [0, 255, 6, 12, 14, 73, 146, 37]))
 
     D = 128
     # one token: out = v exactly
@@ -95,6 +105,23 @@ def _quant_zero_sign(X, bits):
     return c, s, ((2 ** bits - 1) - z).astype(np.uint8)
 
 
+def _quant_reciprocal(X, bits):
+    """The rule with x * (1/s) in place of the division x / s."""
+    Bq = np.float32(2 ** bits - 1)
+    x = X.astype(np.float32)
+    lo = np.minimum(x.min(axis=-1), np.float32(0))
+    hi = np.maximum(x.max(axis=-1), np.float32(0))
+    r = hi - lo
+    r = np.where(r == np.float32(0), Bq, r)
+    s16 = np.maximum((r / Bq).astype(np.float16), np.float16(2.0 ** -24))
+    sf = s16.astype(np.float32)
+    z = np.clip(np.rint(-lo / sf), 0, Bq).astype(np.float32)
+    q = np.clip(np.rint(x * (np.float32(1) / sf)[..., None]) + z[..., None], 0, Bq).astype(np.uint8)
+    if bits == 4:
+        q = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    return q, s16, z.astype(np.uint8)
+
+
 def _attn_no_scale(Q, K, V, lengths):
     return kv.decode_attention(np.asarray(Q) * np.sqrt(Q.shape[-1]), K, V, lengths)
 
@@ -115,8 +142,9 @@ def _attn_length_plus_one(Q, K, V, lengths):
 
 @pytest.mark.parametrize("quantize,attention", [
     (_quant_swapped_nibbles, kv.decode_attention), (_quant_zero_sign, kv.decode_attention),
+    (_quant_reciprocal, kv.decode_attention),
     (kv.quantize, _attn_no_scale), (kv.quantize, _attn_head_modulo), (kv.quantize, _attn_length_plus_one)],
-    ids=["nibble_order", "zero_sign", "no_sqrt_d", "head_modulo", "length_off_by_one"])
+    ids=["nibble_order", "zero_sign", "reciprocal", "no_sqrt_d", "head_modulo", "length_off_by_one"])
 def test_pins_reject_planted_mistakes(quantize, attention):
     res = pins(quantize, attention)
     assert not all(res.values()), res

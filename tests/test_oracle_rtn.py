@@ -1,7 +1,9 @@
 """Pins of the round-to-nearest INT4 quantisation oracle (oracle/rtn.py),
 independent of the oracle's own code: exact recovery of weights that lie on a
 quantisation grid, the RTN error bound, the degenerate groups, hand-worked
-ties, and planted mistakes that each pin set must reject."""
+ties (also at a scale whose binary32 reciprocal is inexact, which tells the
+per-weight division from a multiplication by 1/s), and planted mistakes that
+each pin set must reject."""
 import numpy as np
 import pytest
 
@@ -62,6 +64,18 @@ def pins(quantize):
     q, z, s = quantize(np.repeat(T, 16, axis=1), 8)
     out["ties"] = bool(float(s[0, 0]) == 1.0 and z[0, 0] == 8
                        and np.all(q[:, 0] == np.array([0, 15, 10, 12, 8, 2, 8, 9])))
+
+    # exact ties at a scale whose reciprocal is inexact in binary32: the group
+    # max 0.150146484375 = 1230 * 2^-13 gives s = hi / 15 = 1025 * 2^-17 =
+    # 0.010009765625 (fp16 bits 0x2120) exactly, z = 0; w = 3.5 s, 7.5 s and
+    # 13.5 s are fp16 values, w / s is exactly the half-integer and rounds to
+    # the even code 4, 8, 14 (w * fl(1/s) lands just below each and would give
+    # 3, 7, 13); 0.01, 0.06 and 0.1 (as fp16) divide to 0.9985, 5.994, 9.988.
+    H = np.array([0.0, 0.150146484375, 0.0350341796875, 0.0750732421875, 0.1351318359375, 0.01, 0.06, 0.1],
+                 dtype=np.float16).reshape(8, 1)
+    q, z, s = quantize(np.repeat(H, 16, axis=1), 8)
+    out["ties_inexact_reciprocal"] = bool(s.view(np.uint16)[0, 0] == 0x2120 and z[0, 0] == 0
+                                          and np.all(q[:, 0] == np.array([0, 15, 4, 8, 14, 1, 6, 10])))
     return out
 
 
@@ -87,17 +101,17 @@ def _mutant(kind):
         zz = rnd((lo if kind == "zero_sign" else -lo) / sf)
         z = np.clip(zz, 0, 15)
         top = 16 if kind == "clamp_16" else 15
-        inv = np.float32(1) / sf
-        q = np.clip(rnd(w * inv[:, None, :]) + z[:, None, :], 0, top)
+        quot = w * (np.float32(1) / sf)[:, None, :] if kind == "reciprocal" else w / sf[:, None, :]
+        q = np.clip(rnd(quot) + z[:, None, :], 0, top)
         if kind == "round_half_up":
-            q = np.clip(np.floor(w * inv[:, None, :] + 0.5) + z[:, None, :], 0, 15)
+            q = np.clip(np.floor(quot + 0.5) + z[:, None, :], 0, 15)
             z = np.clip(np.floor(-lo / sf + 0.5), 0, 15)
         return q.reshape(K, N).astype(np.uint8), z.astype(np.uint8), s16
     return quantize
 
 
 @pytest.mark.parametrize("kind", ["no_zero_in_range", "divide_by_16", "floor", "zero_sign", "clamp_16",
-                                  "round_half_up"])
+                                  "round_half_up", "reciprocal"])
 def test_pins_reject_planted_mistakes(kind):
     res = pins(_mutant(kind))
     assert not all(res.values()), (kind, res)

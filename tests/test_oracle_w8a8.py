@@ -38,6 +38,14 @@ def pins(quantize_act, gemm):
     Z[1, 3] = np.float16(-0.5)
     qz, sz = quantize_act(Z)
     out["zero_row"] = bool(sz[0] == 1.0 and not qz[0].any() and qz[1, 3] == -127)
+    # division, not multiplication by the reciprocal: a = 0.50146484375 (fp16
+    # bits 0x3803) gives s = fl32(a / 127) = 0.0039485423; x = a / 2 divides to
+    # fl32(x / s) = 63.499996 -> 63 (and -63), while x * fl32(1/s) rounds to
+    # exactly 63.5 and would give the even 64; 0.125 / s = 31.66 -> 32.
+    R = np.array([[0.50146484375, 0.250732421875, -0.250732421875, 0.125]], dtype=np.float16)
+    qr, sr = quantize_act(R)
+    out["division_not_reciprocal"] = bool(np.array_equal(qr[0], [127, 63, -63, 32])
+                                          and sr[0] == np.float32(0.50146484375) / np.float32(127))
 
     # brute force on a tiny product
     qx = rng.integers(-127, 128, size=(3, 7)).astype(np.int8)
@@ -106,6 +114,13 @@ def _quant_no_zero_guard(X):
     return np.clip(q, -127, 127).astype(np.int8), s
 
 
+def _quant_reciprocal(X):
+    x = X.astype(np.float32)
+    a = np.abs(x).max(axis=1)
+    s = np.where(a == 0, np.float32(1), a / np.float32(127)).astype(np.float32)
+    return np.clip(np.rint(x * (np.float32(1) / s)[:, None]), -127, 127).astype(np.int8), s
+
+
 def _gemm_transposed(qx, sx, qw, sw, rows=None):
     if qw.shape[0] == qw.shape[1]:
         qw = qw.T
@@ -123,8 +138,8 @@ def _gemm_float_acc(qx, sx, qw, sw, rows=None):
 
 @pytest.mark.parametrize("quantize,gemm", [
     (_quant_amax_128, w8.gemm), (_quant_trunc, w8.gemm), (_quant_no_zero_guard, w8.gemm),
-    (w8.quantize_act, _gemm_no_sx), (w8.quantize_act, _gemm_float_acc)],
-    ids=["scale_128", "truncation", "zero_row", "missing_sx", "float32_accumulation"])
+    (_quant_reciprocal, w8.gemm), (w8.quantize_act, _gemm_no_sx), (w8.quantize_act, _gemm_float_acc)],
+    ids=["scale_128", "truncation", "zero_row", "reciprocal", "missing_sx", "float32_accumulation"])
 def test_pins_reject_planted_mistakes(quantize, gemm):
     res = pins(quantize, gemm)
     assert not all(res.values()), res
