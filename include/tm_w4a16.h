@@ -98,8 +98,11 @@ tm_status tm_packed_info(const tm_packed* p, int* K, int* N, int* g, size_t* byt
  * round-to-nearest-even at each step:
  *   lo = min(0, min w), hi = max(0, max w); r = hi - lo, or 15 if r == 0
  *   s[G][n] = fp16(r / 15), at least 2^-24 (the smallest positive fp16)
- *   z[G][n] = clamp(rint(-lo / s), 0, 15);  i = 1 / s (once per group and column)
- *   q[k][n] = clamp(rint(w[k][n] * i) + z, 0, 15)
+ *   z[G][n] = clamp(rint(-lo / s), 0, 15)
+ *   q[k][n] = clamp(rint(w[k][n] / s) + z, 0, 15)
+ * (the division per weight is computed as a multiply by 1/s and one fma
+ * correction, which gives the quotient's integer rounding exactly, ties
+ * included, for fp16 w and s)
  *   W : device, fp16 bits [K][N] row-major, 16-byte aligned
  *   q : device, uint8 [K][N] (one code per byte), 8-byte aligned
  *   z : device, uint8 [K/g][N], 8-byte aligned;  s: device, fp16 bits [K/g][N], 16-byte aligned
@@ -119,8 +122,8 @@ tm_status tm_quantize_rtn(const uint16_t* W, int K, int N, int g, uint8_t* q, ui
  * D = 64, 128 or 256) -> codes, an fp16 scale and a uint8 zero per vector, by
  * the rule of tm_quantize_rtn with B = 2^bits - 1 in place of 15:
  *   lo = min(0, min x), hi = max(0, max x); r = hi - lo, or B if r == 0;
- *   s = fp16(r / B) (>= 2^-24); z = clamp(rint(-lo / s), 0, B); i = 1 / s;
- *   q = clamp(rint(x * i) + z, 0, B)          (IEEE binary32, ties to even)
+ *   s = fp16(r / B) (>= 2^-24); z = clamp(rint(-lo / s), 0, B);
+ *   q = clamp(rint(x / s) + z, 0, B)          (IEEE binary32, ties to even)
  *   X     : device fp16 [rows][D], 4-byte aligned
  *   codes : device uint8 [rows][D] (bits 8) or [rows][D/2] (bits 4, even
  *           index in the low nibble); s: fp16 [rows]; z: uint8 [rows]

@@ -8,7 +8,7 @@
  * per output channel; both symmetric, in IEEE binary32 with
  * round-to-nearest-even at each step:
  *   a = max |x| over the row (column);  s = a / 127, or 1 when a == 0
- *   i = 1 / s;  q = clamp(rint(x * i), -127, 127)
+ *   q = clamp(rint(x / s), -127, 127)          (one division per value)
  *   Y[m][n] = fp16( s_x[m] * s_w[n] * sum_k q_x[m][k] q_w[k][n] )
  * The integer products are exact on the tensor cores (fp16 operands holding
  * the integers, fp32 accumulation: exact while a partial sum stays below

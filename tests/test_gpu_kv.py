@@ -43,6 +43,21 @@ def test_kv_quantize_bit_exact(bits, D):
     assert np.array_equal(c.cpu().numpy(), c0)
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+def test_kv_quantize_exact_ties_bit_exact(bits):
+    """Vectors holding, for one fp16 scale each, the maximum B s and every
+    exact tie (k + 1/2) s that is an fp16 value: the codes equal the division
+    rule's (a multiply by fl(1/s) would round some ties the wrong way)."""
+    from tests.test_gpu_rtn import tie_columns
+    X = np.ascontiguousarray(tie_columns(2 ** bits - 1, 128, count=1024).T)  # [vectors][D = 128]
+    c, s, z = binding.kv_quantize(_dev(X.view(np.uint16)).view(torch.float16), bits)
+    torch.cuda.synchronize()
+    c0, s0, z0 = kv.quantize(X, bits)
+    assert np.array_equal(s.cpu().numpy().view(np.uint16), s0.view(np.uint16))
+    assert np.array_equal(z.cpu().numpy(), z0)
+    assert np.array_equal(c.cpu().numpy(), c0)
+
+
 def _hm(a):
     """[B][L][Hkv](...) -> the head-major cache order [B][Hkv][L](...)."""
     return np.ascontiguousarray(np.swapaxes(a, 1, 2))

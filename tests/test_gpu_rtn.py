@@ -92,3 +92,44 @@ def test_rtn_one_launch():
     binding.quantize_rtn(W, 64)
     assert binding.last_launch_count() == 1
     torch.cuda.synchronize()
+
+
+def tie_columns(B, rows, first=0x1C00, count=4096):
+    """Columns that each hold, for one fp16 scale s (s = hi / B exactly, hi an
+    fp16 value), the group maximum hi and every exact tie (k + 1/2) s that is
+    itself an fp16 value; the remaining rows are zeros.  Built on the host from
+    fp16 bit patterns: the quotient of every tie by s is exactly a half-integer,
+    the case where a multiply by the reciprocal 1/s can round to the wrong
+    neighbour."""
+    cols = []
+    for bits in range(first, first + 8 * count):
+        s = np.array([bits], dtype=np.uint16).view(np.float16)[0]
+        hi = np.float16(B * float(s))
+        if float(hi) != B * float(s) or not np.isfinite(hi):
+            continue
+        if np.float16(np.float32(hi) / np.float32(B)) != s:
+            continue
+        ties = [np.float16((k + 0.5) * float(s)) for k in range(B)]
+        ties = [t for k, t in enumerate(ties) if float(t) == (k + 0.5) * float(s)]
+        col = np.zeros(rows, dtype=np.float16)
+        vals = [hi] + ties[: rows - 1]
+        col[: len(vals)] = vals
+        cols.append(col)
+        if len(cols) == count:
+            break
+    cols = cols[: len(cols) // 16 * 16]  # N % 16 == 0
+    return np.ascontiguousarray(np.stack(cols, axis=1))
+
+
+@pytest.mark.parametrize("g", [16, 64, 128])
+def test_rtn_exact_ties_bit_exact(g):
+    """Exact ties w = (k + 1/2) s over a few thousand scales, through the
+    generic (g = 16) and the tiled (g = 64, 128) kernels: the codes equal the
+    division rule's, and the set is one where a plain multiply by fl(1/s)
+    would differ (checked on the host with that rule)."""
+    W = tie_columns(15, g, count=2048)
+    _assert_bit_exact(W, g)
+    w = W.astype(np.float32)
+    _, _, s0 = rtn.quantize(W, g)
+    recip = np.rint(w * (np.float32(1) / s0.astype(np.float32)))
+    assert np.count_nonzero(recip != np.rint(w / s0.astype(np.float32))) > 0

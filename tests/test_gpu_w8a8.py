@@ -77,6 +77,44 @@ def test_quantize_act_bit_exact(M, K):
     assert np.array_equal(xq.cpu().numpy(), q0)
 
 
+def near_tie_rows(count=1024, first=0x3400):
+    """Rows whose maximum a runs over consecutive fp16 values, holding the fp16
+    values nearest to +-(k + 1/2) s for s = fl32(a / 127), k = 0..126: quotients
+    at or within a few ulps of a half-integer, where a multiply by fl32(1/s)
+    rounds some codes differently from the division."""
+    rows = []
+    for bits in range(first, first + count):
+        a = np.array([bits], dtype=np.uint16).view(np.float16)[0]
+        s = np.float32(a) / np.float32(127)
+        v = [a] + [np.float16((k + 0.5) * float(s)) for k in range(127)]
+        rows.append(np.array(v + [-x for x in v[1:]] + [np.float16(0)], dtype=np.float16))
+    return np.stack(rows)
+
+
+def test_quantize_act_near_ties_bit_exact():
+    X = near_tie_rows()
+    for f16 in (False, True):
+        quant = binding.w8a8_quantize_act_f16 if f16 else binding.w8a8_quantize_act
+        xq, sx = quant(torch.from_numpy(X.view(np.uint16)).cuda().view(torch.float16))
+        torch.cuda.synchronize()
+        q0, s0 = w8.quantize_act(X)
+        got = xq.cpu().numpy().astype(np.float32).astype(np.int8) if f16 else xq.cpu().numpy()
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), s0.view(np.uint32))
+        assert np.array_equal(got, q0)
+    x = X.astype(np.float32)
+    recip = np.clip(np.rint(x * (np.float32(1) / s0)[:, None]), -127, 127)
+    assert np.count_nonzero(recip != q0) > 0  # the set separates the two rules
+
+
+def test_quantize_weight_near_ties_bit_exact():
+    W = np.ascontiguousarray(near_tie_rows(count=512).T)  # [K = 256][N = 512]: one channel per row above
+    q, sw = binding.w8_quantize_weight(torch.from_numpy(W.view(np.uint16)).cuda().view(torch.float16))
+    torch.cuda.synchronize()
+    q0, s0 = w8.quantize_weight(W)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), s0.view(np.uint32))
+    assert np.array_equal(q.cpu().numpy(), q0)
+
+
 @pytest.mark.parametrize("K,N", [(1040, 272), (4096, 512), (128, 16)])
 def test_pack_roundtrip(K, N):
     q, s = _weights(K, N)

@@ -15,7 +15,8 @@
 // one IEEE binary32 operation with round-to-nearest-even):
 //   lo = min(0, min x), hi = max(0, max x); r = hi - lo, or B if r == 0
 //   s = fp16(r / B), at least 2^-24;  z = clamp(rint(-lo / s), 0, B)
-//   i = 1 / s;  q = clamp(rint(x * i) + z, 0, B)
+//   q = clamp(rint(x / s) + z, 0, B)   (the division as fp16_quotient: a
+//   reciprocal per vector and one fma correction, ties included)
 // Codes: one byte each (int8) or two per byte, even index in the low nibble
 // (int4); s fp16 and z uint8 per (token, head).
 //
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(128) kv_quant_kernel(const __half* __restrict_
   const float inv = __fdiv_rn(1.f, sf);
   uint32_t c[EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) c[e] = (uint32_t)fminf(fmaxf(rintf(__fmul_rn(v[e], inv)) + zf, 0.f), kB);
+  for (int e = 0; e < EPL; ++e) c[e] = (uint32_t)fminf(fmaxf(rintf(fp16_quotient(v[e], sf, inv)) + zf, 0.f), kB);
   if constexpr (BITS == 8) {
     uint8_t* out = codes + row * D + lane * EPL;
 #pragma unroll
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(128) kv_append_kernel(const __half* __restrict
     const float inv = __fdiv_rn(1.f, sf);
     uint32_t c[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) c[e] = (uint32_t)fminf(fmaxf(rintf(__fmul_rn(v[e], inv)) + zf, 0.f), kB);
+    for (int e = 0; e < 4; ++e) c[e] = (uint32_t)fminf(fmaxf(rintf(fp16_quotient(v[e], sf, inv)) + zf, 0.f), kB);
     if (which == 0) {
       if constexpr (BITS == 8) {
         *reinterpret_cast<uint32_t*>(kc + row * RB + 4 * lane) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);

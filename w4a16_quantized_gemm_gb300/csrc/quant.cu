@@ -6,10 +6,11 @@
 // For every group G of g rows along K and column n (w read as exact binary32):
 //   lo = min(0, min w), hi = max(0, max w); r = hi - lo, or 15 if r == 0
 //   s = fp16(r / 15), at least 2^-24;  z = clamp(rint(-lo / s), 0, 15)
-//   i = 1 / s;  q = clamp(rint(w * i) + z, 0, 15)
+//   q = clamp(rint(w / s) + z, 0, 15)
 // each step one IEEE binary32 operation, round to nearest even, so the codes
-// do not depend on how the work is split (one reciprocal per group and column
-// keeps the per-weight work at a multiply).
+// do not depend on how the work is split.  The division per weight is a
+// multiply by the reciprocal, computed once per group and column, plus one
+// fma correction (fp16_quotient): the same codes as a division, ties included.
 //
 // HBM-bound: 2 bytes read and 1 byte written per weight.
 // g = 64 and 128 (rtn_tma_kernel): a persistent grid, two CTAs per SM, walks
@@ -46,27 +47,28 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[kCols]) {
   }
 }
 
-// Eight codes clamp(rint(f * inv) + z, 0, 15) as bytes.  rint by the
+// Eight codes clamp(rint(f / s) + z, 0, 15) as bytes.  rint by the
 // round-to-nearest-even of an IEEE add: for |x| < 2^22, x + 1.5 * 2^23 is
 // 1.5 * 2^23 + rint(x) exactly, the integer in the low mantissa bits; the
 // zero point and the clamp stay in that biased range (all exact), and the
 // byte is the low bits of the pattern (no float-to-int conversion).
-__device__ __forceinline__ uint2 rtn_codes(const float (&f)[kCols], const float (&inv)[kCols],
-                                           const float (&zf)[kCols]) {
+__device__ __forceinline__ uint2 rtn_codes(const float (&f)[kCols], const float (&sf)[kCols],
+                                           const float (&inv)[kCols], const float (&zf)[kCols]) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
   uint32_t u[kCols];
 #pragma unroll
   for (int c = 0; c < kCols; ++c) {
-    const float t = __fadd_rn(__fadd_rn(__fmul_rn(f[c], inv[c]), kMagic), zf[c]);
+    const float t = __fadd_rn(__fadd_rn(fp16_quotient(f[c], sf[c], inv[c]), kMagic), zf[c]);
     u[c] = __float_as_uint(fminf(fmaxf(t, kMagic), kMagic + 15.f));
   }
   return make_uint2(__byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u),
                     __byte_perm(__byte_perm(u[4], u[5], 0x0040u), __byte_perm(u[6], u[7], 0x0040u), 0x5410u));
 }
 
-// Per column: s (fp16 bits), z and 1/s from the group's lo and hi (the rule above).
-__device__ __forceinline__ void rtn_params(const float (&lo)[kCols], const float (&hi)[kCols], float (&inv)[kCols],
-                                           float (&zf)[kCols], uint32_t (&sbits)[4], uint32_t& zlo, uint32_t& zhi) {
+// Per column: s (fp16 bits and value), z and 1/s from the group's lo and hi (the rule above).
+__device__ __forceinline__ void rtn_params(const float (&lo)[kCols], const float (&hi)[kCols], float (&sfv)[kCols],
+                                           float (&inv)[kCols], float (&zf)[kCols], uint32_t (&sbits)[4],
+                                           uint32_t& zlo, uint32_t& zhi) {
   const __half tiny = __ushort_as_half((unsigned short)1);  // 2^-24, the smallest positive fp16
 #pragma unroll
   for (int c = 0; c < 4; ++c) sbits[c] = 0;
@@ -79,6 +81,7 @@ __device__ __forceinline__ void rtn_params(const float (&lo)[kCols], const float
     if (__half2float(sh) < __half2float(tiny)) sh = tiny;
     const float sf = __half2float(sh);
     zf[c] = fminf(fmaxf(rintf(__fdiv_rn(-lo[c], sf)), 0.f), 15.f);
+    sfv[c] = sf;
     inv[c] = __fdiv_rn(1.f, sf);
     sbits[c >> 1] |= (uint32_t)__half_as_ushort(sh) << (16 * (c & 1));
     if (c < 4) zlo |= (uint32_t)zf[c] << (8 * c);
@@ -126,15 +129,15 @@ __global__ void __launch_bounds__(kQuantThreads) rtn_kernel(const uint4* __restr
       lo[c] = fminf(lo[c], s_lo[y][tx][c]);
       hi[c] = fmaxf(hi[c], s_hi[y][tx][c]);
     }
-  float inv[kCols], zf[kCols];
+  float sfv[kCols], inv[kCols], zf[kCols];
   uint32_t sbits[4], zlo, zhi;
-  rtn_params(lo, hi, inv, zf, sbits, zlo, zhi);
+  rtn_params(lo, hi, sfv, inv, zf, sbits, zlo, zhi);
   uint2* qr = q + (size_t)grp * g * N8 + c8;
 #pragma unroll 16
   for (int k = ty; k < g; k += kRowSlices) {
     float f[kCols];
     unpack8(w[(size_t)k * N8], f);
-    qr[(size_t)k * N8] = rtn_codes(f, inv, zf);
+    qr[(size_t)k * N8] = rtn_codes(f, sfv, inv, zf);
   }
   if (ty == 0) {
     z[(size_t)grp * N8 + c8] = make_uint2(zlo, zhi);
@@ -155,15 +158,15 @@ struct RtnTmaShape {
   static constexpr uint32_t TILE = G * kTmaCols * 2;          // fp16 tile bytes
   static constexpr uint32_t RED_OFF = kTmaStages * TILE;      // [2 parity][2 lo/hi][warps][128] fp16
   static constexpr uint32_t RED = 2 * 2 * kTmaWarps * kTmaCols * 2;
-  static constexpr uint32_t PAR_OFF = RED_OFF + RED;          // [2 parity][2 inv/zero][128] fp32
-  static constexpr uint32_t PAR = 2 * 2 * kTmaCols * 4;
+  static constexpr uint32_t PAR_OFF = RED_OFF + RED;          // [2 parity][inv, zero, s][128] fp32
+  static constexpr uint32_t PAR = 2 * 3 * kTmaCols * 4;
   static constexpr uint32_t BAR_OFF = PAR_OFF + PAR;          // full[S], empty[S], red[2], par[2], abort
   static constexpr uint32_t SMEM = BAR_OFF + 8 * (2 * kTmaStages + 4) + 16 + 128;  // + alignment slack
 };
 
 // One column's scale, zero point and reciprocal from the group's lo and hi
 // (the rule in the header comment).
-__device__ __forceinline__ void rtn_params1(float lo, float hi, float& inv, float& zf, __half& sh) {
+__device__ __forceinline__ void rtn_params1(float lo, float hi, float& sfv, float& inv, float& zf, __half& sh) {
   const __half tiny = __ushort_as_half((unsigned short)1);  // 2^-24, the smallest positive fp16
   float r = hi - lo;
   if (r == 0.f) r = 15.f;
@@ -171,16 +174,18 @@ __device__ __forceinline__ void rtn_params1(float lo, float hi, float& inv, floa
   if (__half2float(sh) < __half2float(tiny)) sh = tiny;
   const float sf = __half2float(sh);
   zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.f), 15.f);
+  sfv = sf;
   inv = __fdiv_rn(1.f, sf);
 }
 
 // Four codes (the magic-constant rounding of rtn_codes) as the bytes of a word.
-__device__ __forceinline__ uint32_t rtn_codes4(const float (&f)[4], const float (&inv)[4], const float (&zf)[4]) {
+__device__ __forceinline__ uint32_t rtn_codes4(const float (&f)[4], const float (&sf)[4], const float (&inv)[4],
+                                               const float (&zf)[4]) {
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
   uint32_t u[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const float t = __fadd_rn(__fadd_rn(__fmul_rn(f[c], inv[c]), kMagic), zf[c]);
+    const float t = __fadd_rn(__fadd_rn(fp16_quotient(f[c], sf[c], inv[c]), kMagic), zf[c]);
     u[c] = __float_as_uint(fminf(fmaxf(t, kMagic), kMagic + 15.f));
   }
   return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u);
@@ -262,7 +267,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
   // Per tile: rows into registers and the slot released; column minima and
   // maxima per warp (half2, exact) into shared memory; warp w then finishes
   // columns 16 w .. 16 w + 15 (one per lane: the three divisions of the rule
-  // once per column) and publishes 1/s and z; every lane codes its 4 columns.
+  // once per column) and publishes s, 1/s and z; every lane codes its 4 columns.
   // Both exchanges are double-buffered by tile parity behind mbarriers.
   constexpr int R = SH::ROWS;
   __half* red = reinterpret_cast<__half*>(smem + SH::RED_OFF);
@@ -299,8 +304,9 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
     if (!mbar_wait(red_bar(pb), (uint32_t)(it >> 1) & 1u, abort_flag, &s_err_rtn)) break;
     const int t = (int)blockIdx.x + it * (int)gridDim.x;
     const int grp = t / NB, col0 = (t % NB) * kTmaCols;
-    float* p_inv = par + (pb * 2 + 0) * kTmaCols;
-    float* p_zf = par + (pb * 2 + 1) * kTmaCols;
+    float* p_inv = par + (pb * 3 + 0) * kTmaCols;
+    float* p_zf = par + (pb * 3 + 1) * kTmaCols;
+    float* p_sf = par + (pb * 3 + 2) * kTmaCols;
     if (lane < 16) {
       const int c = 16 * warp + lane;
       __half lo = red_lo[c], hi = red_hi[c];
@@ -309,11 +315,12 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
         lo = __hmin(lo, red_lo[w * kTmaCols + c]);
         hi = __hmax(hi, red_hi[w * kTmaCols + c]);
       }
-      float inv, zf;
+      float sfv, inv, zf;
       __half sh;
-      rtn_params1(__half2float(lo), __half2float(hi), inv, zf, sh);
+      rtn_params1(__half2float(lo), __half2float(hi), sfv, inv, zf, sh);
       p_inv[c] = inv;
       p_zf[c] = zf;
+      p_sf[c] = sfv;
       if (col0 + c < N) {
         z[(size_t)grp * N + col0 + c] = (uint8_t)zf;
         s[(size_t)grp * N + col0 + c] = sh;
@@ -326,13 +333,15 @@ __global__ void __launch_bounds__(kTmaThreads, 2) rtn_tma_kernel(const __grid_co
     if (col < N) {
       const float4 i4 = *reinterpret_cast<const float4*>(p_inv + 4 * lane);
       const float4 z4 = *reinterpret_cast<const float4*>(p_zf + 4 * lane);
+      const float4 s4 = *reinterpret_cast<const float4*>(p_sf + 4 * lane);
       const float inv[4] = {i4.x, i4.y, i4.z, i4.w}, zf[4] = {z4.x, z4.y, z4.z, z4.w};
+      const float sf[4] = {s4.x, s4.y, s4.z, s4.w};
       uint8_t* qr = q + ((size_t)grp * G + warp * R) * N + col;
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         float f[4];
         unpack4(v[r], f);
-        *reinterpret_cast<uint32_t*>(qr + (size_t)r * N) = rtn_codes4(f, inv, zf);
+        *reinterpret_cast<uint32_t*>(qr + (size_t)r * N) = rtn_codes4(f, sf, inv, zf);
       }
     }
   }

@@ -91,6 +91,21 @@ struct tm_packed {
 
 namespace w4 {
 
+// w / s for the quantisers' rounding rule, q = rint(w / s), from the
+// reciprocal i = fl(1/s) computed once per scale: t = w i, the remainder
+// w - t s by one fma, and one correction t + (w - t s) i by another.  For fp16
+// w and s (the weight and KV quantisers) rint of the result equals rint of the
+// exact quotient: at a half-integer quotient h the correction lands on h
+// itself (the remaining error is below 2^-46 h), and any other quotient of two
+// fp16 values lies at least 1/8188 from every half-integer, far more than the
+// result's error of about one binary32 ulp.  w * i alone can miss an exact
+// tie by an ulp and round it the wrong way.
+__device__ __forceinline__ float fp16_quotient(float w, float s, float i) {
+  const float t = __fmul_rn(w, i);
+  const float r = __fmaf_rn(-t, s, w);
+  return __fmaf_rn(r, i, t);
+}
+
 // Device-side sticky error bits (per device; read by tm_device_error).
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrBadCode = 2u;

@@ -7,8 +7,9 @@
 //   activations per token (row m), dynamic and symmetric, weights per output
 //   channel (column n), symmetric, each in IEEE binary32 with
 //   round-to-nearest-even:
-//     a = max |x|;  s = a / 127, or 1 when a == 0;  i = 1 / s;
-//     q = clamp(rint(x * i), -127, 127)
+//     a = max |x|;  s = a / 127, or 1 when a == 0;
+//     q = clamp(rint(x / s), -127, 127)     (an IEEE division per value: s is
+//     a binary32 value, and x * (1/s) can round a code differently)
 //   Y[m][n] = s_x[m] s_w[n] sum_k q_x[m][k] q_w[k][n]
 //
 // GB300 design.  The int8 tensor-core rate of this part is far below its fp16
@@ -95,7 +96,6 @@ __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restr
 #pragma unroll
   for (int w = 1; w < 8; ++w) a = fmaxf(a, red[w]);
   const float s = a == 0.f ? 1.f : __fdiv_rn(a, 127.f);
-  const float inv = __fdiv_rn(1.f, s);
   if (threadIdx.x == 0) sx[m] = s;
   for (int i = threadIdx.x; i < nv; i += 256) {
     const uint4 v = row[i];
@@ -104,8 +104,8 @@ __global__ void __launch_bounds__(256) w8_quant_act_kernel(const __half* __restr
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-      c[2 * e] = fminf(fmaxf(rintf(__fmul_rn(f.x, inv)), -127.f), 127.f);
-      c[2 * e + 1] = fminf(fmaxf(rintf(__fmul_rn(f.y, inv)), -127.f), 127.f);
+      c[2 * e] = fminf(fmaxf(rintf(__fdiv_rn(f.x, s)), -127.f), 127.f);
+      c[2 * e + 1] = fminf(fmaxf(rintf(__fdiv_rn(f.y, s)), -127.f), 127.f);
     }
     if (F16) {
       // integers of magnitude <= 127: exact in fp16
@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(256) w8_wquant_kernel(const __half* __restrict
   const int c8 = blockIdx.x * 32 + tx, N8 = N / 8;
   if (c8 >= N8) return;
   const int k0 = blockIdx.y * kWqRows, k1 = min(K, k0 + kWqRows);
-  float inv[8];
+  float sc[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) inv[c] = __fdiv_rn(1.f, w8_scale_of(amax[8 * c8 + c]));
+  for (int c = 0; c < 8; ++c) sc[c] = w8_scale_of(amax[8 * c8 + c]);
   for (int k = k0 + ty; k < k1; k += 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(W + (size_t)k * N + 8 * c8);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(256) w8_wquant_kernel(const __half* __restrict
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-      b[2 * e] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.x, inv[2 * e])), -127.f), 127.f) & 0xFFu;
-      b[2 * e + 1] = (uint32_t)(int)fminf(fmaxf(rintf(__fmul_rn(f.y, inv[2 * e + 1])), -127.f), 127.f) & 0xFFu;
+      b[2 * e] = (uint32_t)(int)fminf(fmaxf(rintf(__fdiv_rn(f.x, sc[2 * e])), -127.f), 127.f) & 0xFFu;
+      b[2 * e + 1] = (uint32_t)(int)fminf(fmaxf(rintf(__fdiv_rn(f.y, sc[2 * e + 1])), -127.f), 127.f) & 0xFFu;
     }
     *reinterpret_cast<uint2*>(q + (size_t)k * N + 8 * c8) =
         make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24), b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
