@@ -122,6 +122,22 @@ def test_decode_stage_override(stages):
     assert err <= TOL, err
 
 
+def test_decode_plan_rejects_bad_settings():
+    """Launch settings of the decode kernel outside the served set are refused
+    with a status (invalid argument or unsupported), never clamped."""
+    w = packed(2048, 512, 128)
+    bad = [({"warp_n": 3}, 8, 1), ({"warp_n": 8}, 8, 1), ({"tile_n": 96}, 8, 1), ({"tile_n": 32}, 8, 1),
+           ({"stages": 1}, 8, 1), ({"stages": 9}, 8, 1), ({"split_k": 3}, 8, 1), ({"split_k": 16}, 8, 1),
+           ({"warp_n": 4}, 32, 3), ({"warp_n": 4, "tile_n": 256}, 32, 3), ({"warp_n": 2, "tile_n": 64}, 64, 3)]
+    for cfg, M, status in bad:
+        with pytest.raises(binding.TMError) as e:
+            binding.plan(w, M, dict(cfg, path=1))
+        assert e.value.status == status, (cfg, M, e.value.status)
+    # a served combination comes back as asked
+    c = binding.plan(w, 8, {"path": 1, "warp_n": 2, "tile_n": 128, "stages": 3, "split_k": 2})
+    assert (c["warp_n"], c["tile_n"], c["stages"], c["split_k"]) == (2, 128, 3, 2)
+
+
 def test_m64_both_paths_agree_with_oracle():
     e1, Y1 = run_and_compare(64, 4096, 1024, 128, config={"path": 1})
     e2, Y2 = run_and_compare(64, 4096, 1024, 128, config={"path": 2})
