@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(128) kv_quant_kernel(const __half* __restrict_
 // ------------------------------------------------------------ attention -----
 
 constexpr int kAttnD = 128;
-constexpr int kConsumers = 8;                    // warps that compute, one 16-token tile of a slot each
+// Seven compute warps and the producer: 8 warps of up to 128 registers, so
+// that two CTAs share an SM (each of the SM's four schedulers holds 16K
+// registers: 4 warps x 128; a ninth warp per CTA would leave one CTA per SM).
+constexpr int kConsumers = 7;                    // warps that compute, one 16-token tile of a slot each
 constexpr int kAttnThreads = 32 * (kConsumers + 1);  // + one producer warp
 constexpr int kSlotTiles = kConsumers;           // 16-token tiles per ring slot
 constexpr int kState = 2 + kAttnD;               // max, sum, 128 accumulators per query head
@@ -670,11 +673,31 @@ __global__ void __launch_bounds__(128) kv_append_kernel(const __half* __restrict
   }
 }
 
+// Launch with S CTAs per (sequence, KV head) along the tokens; S = 0 picks S:
+// split the tokens while the grid still fits in one wave of resident CTAs (the
+// kernel's occupancy, registers included) and every CTA keeps at least four
+// slots of tokens.
 template <int BITS, int G>
 tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
   constexpr uint32_t smem = KvSlot<BITS>::kSmem;
   static std::atomic<unsigned long long> attr_set{0};  // one bit per device
   if (!smem_attr_once(attr_set, (const void*)kv_attn_tc_kernel<BITS, G>, (int)smem)) return TM_ERR_CUDA;
+  if (!S) {
+    const int device = current_device();
+    if (device < 0 || device >= 64) return TM_ERR_CUDA;
+    static std::atomic<int> per_sm_cache[64];  // resident CTAs per SM, per device (0 = not yet queried)
+    int per_sm = per_sm_cache[device].load();
+    if (per_sm == 0) {
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kv_attn_tc_kernel<BITS, G>, kAttnThreads, smem) !=
+              cudaSuccess ||
+          per_sm < 1)
+        return TM_ERR_CUDA;
+      per_sm_cache[device].store(per_sm);
+    }
+    const long long slots = (long long)num_sms(device) * per_sm;
+    S = 1;
+    while (S < kMaxSplit && (long long)B * P.Hkv * S * 2 <= slots && P.L / (2 * S) >= 4 * 16 * kSlotTiles) S *= 2;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(B * P.Hkv), (unsigned)S, 1);
   cfg.blockDim = dim3(kAttnThreads, 1, 1);
@@ -688,14 +711,6 @@ tm_status attn_launch(const AttnParams& P, int B, int S, cudaStream_t stream) {
   cfg.attrs = at;
   cfg.numAttrs = S > 1 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kv_attn_tc_kernel<BITS, G>, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
-}
-
-// CTAs resident on one SM for the attention kernel (shared memory bound).
-int attn_resident(uint32_t smem) {
-  int per_sm = 0, reserved = 0;
-  sm_shared_memory(0, &per_sm, &reserved);
-  const int r = per_sm / (int)(smem + reserved);
-  return r < 1 ? 1 : (r > 2 ? 2 : r);
 }
 
 }  // namespace
@@ -758,15 +773,7 @@ extern "C" tm_status tm_kv_decode_attention(const uint16_t* Q, const uint8_t* kc
                         reinterpret_cast<uintptr_t>(vz);
   if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(out) & 1u)) return TM_ERR_ALIGNMENT;
   if (B == 0) return TM_OK;
-  int S = split;
-  if (!S) {
-    // split the tokens while the grid still fits in one wave of resident CTAs
-    // and every CTA keeps at least four slots of tokens
-    const uint32_t smem = bits == 8 ? KvSlot<8>::kSmem : KvSlot<4>::kSmem;
-    const long long slots = (long long)num_sms(current_device()) * attn_resident(smem);
-    S = 1;
-    while (S < kMaxSplit && (long long)B * Hkv * S * 2 <= slots && L / (2 * S) >= 4 * 16 * kSlotTiles) S *= 2;
-  }
+  const int S = split;
   AttnParams P;
   P.Q = reinterpret_cast<const __half*>(Q);
   P.kc = kc;
