@@ -458,19 +458,24 @@ __global__ void __launch_bounds__((kW8NW + 1) * 32) w8_kernel(const __grid_const
 //     rows of W^T = the CTA's 128 output columns) and one of X (BT rows), both
 //     with the 128-byte swizzle, into a ring; weights of the first slots before
 //     `griddepcontrol.wait`, X after;
-//   * warps 2..9 convert a ring slot into one of two "converted" slots: the
+//   * warps 2..9 convert a ring slot into one of the "converted" slots: the
 //     warp pair of tensor-memory lane quarter q turns rows 32q .. 32q+31 of the
 //     weight box (one 64-k unit each) into fp16 and writes them with
 //     tcgen05.st.32x32b as the MMA's A operand (lane = output column, column c
-//     = k pair c of a 16-k slice); all 256 threads turn the X box into fp16 rows
-//     of 128 bytes with the 128-byte swizzle (the K-major B operand), then
-//     release the ring slot;
+//     = k pair c of a 16-k slice); with int8 X all 256 threads also turn the X
+//     box into fp16 rows of 128 bytes with the 128-byte swizzle (the K-major B
+//     operand); then they release the ring slot;
+//   * with X given as fp16 codes, X has a ring of its own, one 64-k unit (BT
+//     rows x 128 bytes) per slot, each freed by the commit of the MMAs that
+//     read it, so that a weight slot is free as soon as it is converted (three
+//     weight slots, five X units and four tensor-memory A slots at 256-row
+//     tiles; one ring of two 80 KB slots held X and weights before);
 //   * warp 1, one thread: 8 MMAs (M = 128, N = BT, K = 16) per converted slot,
 //     whose commit frees it;
 //   * warps 2..9 again: epilogue, y = acc s_x[m] s_w[n] -> fp16; split K over a
 //     cluster reduces through distributed shared memory in rank order.
 constexpr int kW8TcThreads = 320;
-constexpr int kW8TcConv = 2;  // converted slots (tensor-memory A + fp16 X)
+constexpr int kW8TcConv = 2;  // converted slots with int8 X (tensor-memory A + fp16 X in shared memory)
 
 template <int BT, bool XH>
 struct W8TcShape {
@@ -478,13 +483,18 @@ struct W8TcShape {
   static constexpr uint32_t XR_BYTES = BT * 128;  // one 128-k block of BT int8 rows
   static constexpr uint32_t XF_UNIT = BT * 128;   // fp16 X, one 64-k unit
   static constexpr uint32_t XF_SLOT = 2 * XF_UNIT;
-  // XH: X arrives as fp16 codes (two 64-k units) in the ring slot itself;
-  // otherwise as int8, converted into XF_SLOT-sized buffers of their own.
-  static constexpr uint32_t SLOT = W_BYTES + (XH ? XF_SLOT : XR_BYTES);
+  // XH: X arrives as fp16 codes in a ring of its own, one 64-k unit per slot,
+  // each freed by the MMAs' commit, while the weight ring's slots are freed
+  // as soon as they are converted; otherwise X arrives as int8 next to the
+  // weights and is converted into XF_SLOT-sized buffers of its own.
+  static constexpr uint32_t SLOT = W_BYTES + (XH ? 0 : XR_BYTES);
   static constexpr uint32_t CONV_SLOTS = XH ? 0 : kW8TcConv;  // converted X buffers
+  // converted slots: with fp16 X only tensor-memory A slots, four of them
+  static constexpr int SC = XH ? 4 : kW8TcConv;
   static constexpr uint32_t A_COLS = 64;  // 8 slices of 16 k, 8 columns each
   static constexpr uint32_t A_COL = BT;   // A slots right after the accumulator columns
-  static constexpr uint32_t TMEM_COLS = BT + kW8TcConv * A_COLS <= 256 ? 256 : 512;
+  static constexpr uint32_t TMEM_COLS = BT + SC * A_COLS <= 256 ? 256 : 512;
+  static_assert(BT + SC * A_COLS <= 512, "tensor memory");
   static constexpr int TPR = 256 / BT;     // converter threads per X row
   static constexpr int CPT = 8 / TPR;      // 16-byte X chunks per converter thread
   static_assert(SLOT % 1024 == 0 && XF_UNIT % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -497,6 +507,8 @@ struct W8TcParams {
   int M, N;
   int kb_total, kb_per_cta;
   int stages;       // ring slots
+  int xstages;      // XH: slots of the X ring (64-k units)
+  uint32_t x_off;   // XH: offset of the X ring
   uint32_t xf_off;  // offset of the converted X slots
   uint32_t bar_off;
 };
@@ -511,7 +523,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
     w8tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                 const W8TcParams P) {
   using SH = W8TcShape<BT, XH>;
-  constexpr int SC = kW8TcConv;
+  constexpr int SC = SH::SC;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -526,27 +538,33 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
   const int kb0 = blockIdx.z * P.kb_per_cta;
   const int nkb = max(0, min(P.kb_total, kb0 + P.kb_per_cta) - kb0);
   const int SA = P.stages;
+  const int SX = XH ? P.xstages : 0;
 
   const uint32_t barA = base + P.bar_off;  // [SA] full, then [SA] empty
   const uint32_t barC = barA + 16 * SA;    // [SC] full, then [SC] empty (converted slots)
-  const uint32_t bar_acc = barC + 16 * SC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.bar_off + 16 * SA + 16 * SC + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + 16 * SA + 16 * SC + 12);
+  const uint32_t barX = barC + 16 * SC;    // XH: [SX] full, then [SX] empty (X units)
+  const uint32_t bar_acc = barX + 16 * SX;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + P.bar_off + 16 * (SA + SC + SX) + 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + P.bar_off + 16 * (SA + SC + SX) + 12);
   auto fullA = [&](int s) { return barA + 8 * s; };
   auto emptyA = [&](int s) { return barA + 8 * (SA + s); };
   auto fullC = [&](int s) { return barC + 8 * s; };
   auto emptyC = [&](int s) { return barC + 8 * (SC + s); };
+  auto fullX = [&](int s) { return barX + 8 * s; };
+  auto emptyX = [&](int s) { return barX + 8 * (SX + s); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
       mbar_init(fullA(s), 1);
-      // XH: the slot holds the MMA's B operand and is freed by its commit;
-      // otherwise by the eight converter warps
-      mbar_init(emptyA(s), XH ? 1 : 8);
+      mbar_init(emptyA(s), 8);  // freed by the eight converter warps
     }
     for (int s = 0; s < SC; ++s) {
       mbar_init(fullC(s), 8);
       mbar_init(emptyC(s), 1);
+    }
+    for (int s = 0; s < SX; ++s) {
+      mbar_init(fullX(s), 1);
+      mbar_init(emptyX(s), 1);  // freed by the commit of the MMAs that read it
     }
     mbar_init(bar_acc, 1);
     *abort_flag = 0;
@@ -568,31 +586,45 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
       prefetch_tmap(&tmX);
       prefetch_tmap(&tmW);
       auto issue_w = [&](int i, int s) { tma_load_3d(base + s * SH::SLOT, &tmW, 0, nt0 * 16, kb0 + i, fullA(s)); };
-      auto issue_x = [&](int i, int s) {
-        if (XH) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-            tma_load_2d(base + s * SH::SLOT + SH::W_BYTES + u * SH::XF_UNIT, &tmX, (kb0 + i) * 128 + 64 * u, m0,
-                        fullA(s));
-        } else {
-          tma_load_2d(base + s * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(s));
-        }
-      };
       const int first = min(nkb, SA);
       for (int i = 0; i < first; ++i) {
         mbar_expect_tx(fullA(i), SH::SLOT);
         issue_w(i, i);
       }
       grid_dependency_wait();
-      for (int i = 0; i < first; ++i) issue_x(i, i);
-      int issued = first;
-      for (int i = first; i < nkb; ++i) {
-        const int s = i % SA;
-        if (!mbar_wait(emptyA(s), (uint32_t)(i / SA - 1) & 1u, abort_flag, &s_err_w8)) break;
-        mbar_expect_tx(fullA(s), SH::SLOT);
-        issue_w(i, s);
-        issue_x(i, s);
-        issued = i + 1;
+      int issued = first, issued_x = 0;
+      if constexpr (XH) {
+        // in the order the MMAs consume them: block i's weights, then its two X units
+        auto issue_xu = [&](int j) {
+          const int sx = j % SX;
+          if (j >= SX && !mbar_wait(emptyX(sx), (uint32_t)(j / SX - 1) & 1u, abort_flag, &s_err_w8)) return false;
+          mbar_expect_tx(fullX(sx), SH::XF_UNIT);
+          tma_load_2d(base + P.x_off + sx * SH::XF_UNIT, &tmX, kb0 * 128 + 64 * j, m0, fullX(sx));
+          issued_x = j + 1;
+          return true;
+        };
+        bool ok = true;
+        for (int i = 0; i < nkb && ok; ++i) {
+          if (i >= first) {
+            const int s = i % SA;
+            if (!mbar_wait(emptyA(s), (uint32_t)(i / SA - 1) & 1u, abort_flag, &s_err_w8)) break;
+            mbar_expect_tx(fullA(s), SH::SLOT);
+            issue_w(i, s);
+            issued = i + 1;
+          }
+          ok = issue_xu(2 * i) && issue_xu(2 * i + 1);
+        }
+        for (int j = max(0, issued_x - SX); j < issued_x; ++j) w8_drain(fullX(j % SX), (uint32_t)(j / SX) & 1u);
+      } else {
+        for (int i = 0; i < first; ++i) tma_load_2d(base + i * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(i));
+        for (int i = first; i < nkb; ++i) {
+          const int s = i % SA;
+          if (!mbar_wait(emptyA(s), (uint32_t)(i / SA - 1) & 1u, abort_flag, &s_err_w8)) break;
+          mbar_expect_tx(fullA(s), SH::SLOT);
+          issue_w(i, s);
+          tma_load_2d(base + s * SH::SLOT + SH::W_BYTES, &tmX, (kb0 + i) * 128, m0, fullA(s));
+          issued = i + 1;
+        }
       }
       // never leave with copies in flight into this CTA's shared memory
       for (int i = max(0, issued - SA); i < issued; ++i) w8_drain(fullA(i % SA), (uint32_t)(i / SA) & 1u);
@@ -603,22 +635,33 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(128, BT);
       for (int i = 0; i < nkb; ++i) {
-        const int sc = i % SC, s = i % SA;
+        const int sc = i % SC;
         if (!mbar_wait(fullC(sc), (uint32_t)(i / SC) & 1u, abort_flag, &s_err_w8)) break;
-        // XH: B is the fp16 X that the TMA put in ring slot s (landed before the
-        // converters could finish; the wait is for this thread's own view)
-        if (XH && !mbar_wait(fullA(s), (uint32_t)(i / SA) & 1u, abort_flag, &s_err_w8)) break;
-        tc_fence_after();
-        const uint64_t db = smem_desc_sw128(XH ? base + s * SH::SLOT + SH::W_BYTES : base + P.xf_off + sc * SH::XF_SLOT);
         const uint32_t ta = tmem + SH::A_COL + SH::A_COLS * sc;
+        bool ok = true;
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 2; ++u) {
+          uint64_t db;
+          if constexpr (XH) {
+            // B: the fp16 X of unit 2i + u in the X ring
+            const int j = 2 * i + u, sx = j % SX;
+            if (!mbar_wait(fullX(sx), (uint32_t)(j / SX) & 1u, abort_flag, &s_err_w8)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            db = smem_desc_sw128(base + P.x_off + sx * SH::XF_UNIT);
+          } else {
+            tc_fence_after();
+            db = smem_desc_sw128(base + P.xf_off + sc * SH::XF_SLOT) + (uint64_t)((u * SH::XF_UNIT) >> 4);
+          }
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            tc_mma_f16_ta(tmem, ta + 8u * (4 * u + k), db + (uint64_t)((u * SH::XF_UNIT) >> 4) + (uint64_t)(2 * k),
-                          idesc, (i > 0 || u > 0 || k > 0) ? 1u : 0u);
+            tc_mma_f16_ta(tmem, ta + 8u * (4 * u + k), db + (uint64_t)(2 * k), idesc, (i > 0 || u > 0 || k > 0) ? 1u : 0u);
+          if constexpr (XH) tc_commit(emptyX((2 * i + u) % SX));
+        }
+        if (!ok) break;
         tc_commit(emptyC(sc));
-        if (XH) tc_commit(emptyA(s));
       }
       // completes once every MMA issued above has finished (also on abort)
       tc_commit(bar_acc);
@@ -670,7 +713,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(fullC(sc));
-        if (!XH) mbar_arrive(emptyA(s));
+        mbar_arrive(emptyA(s));
       }
     }
   }
@@ -783,9 +826,10 @@ tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8
 
 // Shared memory of the tensor-memory kernel: ring, converted X slots, barriers, alignment slack.
 template <int BT, bool XH>
-uint32_t w8tc_smem(int stages) {
+uint32_t w8tc_smem(int stages, int xstages) {
   using SH = W8TcShape<BT, XH>;
-  return stages * SH::SLOT + SH::CONV_SLOTS * SH::XF_SLOT + 16 * stages + 16 * kW8TcConv + 16 + 1024;
+  return stages * SH::SLOT + xstages * SH::XF_UNIT + SH::CONV_SLOTS * SH::XF_SLOT +
+         16 * (stages + SH::SC + xstages) + 16 + 1024;
 }
 
 // xq: int8 codes, or (XH) the same codes as fp16 integers.
@@ -802,10 +846,21 @@ tm_status w8tc_run(const void* xq, const float* sx, const tm_w8_packed* p, void*
     S = 1;
     while (S < 8 && (long long)NB * MB * S * 2 <= sms && p->KB / (2 * S) >= 2) S *= 2;
   }
-  int stages = 8;
-  while (stages > 2 && w8tc_smem<BT, XH>(stages) > kW8SmemMax) --stages;
-  const uint32_t smem = w8tc_smem<BT, XH>(stages);
+  // XH: three weight slots and as many 64-k X units as fit (at most 8; two
+  // weight slots for a sixth X unit at 256-row tiles measured no faster);
+  // otherwise as many combined slots as fit
+  int stages = XH ? 3 : 8, xstages = XH ? 8 : 0;
+  if (XH) {
+    while (xstages > 2 && w8tc_smem<BT, XH>(stages, xstages) > kW8SmemMax) --xstages;
+  } else {
+    while (stages > 2 && w8tc_smem<BT, XH>(stages, 0) > kW8SmemMax) --stages;
+  }
+  const uint32_t smem = w8tc_smem<BT, XH>(stages, xstages);
   if (smem > kW8SmemMax) return TM_ERR_UNSUPPORTED;
+  // split K reduces through the shared memory below the barriers: S x (128 / S) columns x BT rows of fp32
+  if (S > 1 && (uint32_t)128 * BT * 4 >
+                   stages * SH::SLOT + xstages * SH::XF_UNIT + SH::CONV_SLOTS * SH::XF_SLOT)
+    return TM_ERR_UNSUPPORTED;
   CUtensorMap tmX;
   {
     EncodeTiledFn fn = encode_tiled_fn();
@@ -829,7 +884,9 @@ tm_status w8tc_run(const void* xq, const float* sx, const tm_w8_packed* p, void*
   P.kb_total = p->KB;
   P.kb_per_cta = (p->KB + S - 1) / S;
   P.stages = stages;
-  P.xf_off = stages * SH::SLOT;
+  P.xstages = xstages;
+  P.x_off = stages * SH::SLOT;
+  P.xf_off = P.x_off + xstages * SH::XF_UNIT;
   P.bar_off = P.xf_off + SH::CONV_SLOTS * SH::XF_SLOT;
   return w8tc_launch_t<BT, XH>(tmX, p->tm_codes, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem,
                                stream);
