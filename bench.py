@@ -554,7 +554,8 @@ def config_detail(wl, stream, peaks, args, min_bytes=300e6, reps=5):
             w.free()
         del copies
         torch.cuda.empty_cache()
-    steps = [_decode_step_at_m(wl, M, stream, peaks) for M in (1, 8, 16, 32)]
+    dwl = wl if wl.kind == "decode" else Workload("decode", device)  # the step figures are the decode workload's
+    steps = [_decode_step_at_m(dwl, M, stream, peaks) for M in (1, 8, 16, 32)]
     out.extend(steps)
     small = [e for e in steps if e["M"] <= 16]
     nb = sum(e["bytes"] for e in small)
@@ -562,7 +563,7 @@ def config_detail(wl, stream, peaks, args, min_bytes=300e6, reps=5):
     out.append({"config": 1, "step": "llama3-8b layer linears at M in {1,8,16} (the decode target's range)",
                 "us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
                 "roofline": roofline_entry(nb, 0, t, peaks)})
-    out.append(_decode_step_concurrent(wl, stream, peaks))
+    out.append(_decode_step_concurrent(dwl, stream, peaks))
     out.append(_prefill_step(device, stream, peaks, max(5, min(args.steps, 50))))
     return out
 
