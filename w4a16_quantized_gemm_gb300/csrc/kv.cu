@@ -30,8 +30,8 @@
 //
 // Attention, one query token per sequence, D = 128, G = Hq / Hkv query heads
 // per KV head: a CTA takes one (sequence, KV head) and a slice of its tokens;
-// a producer warp streams them through a ring of shared-memory slots of 128
-// tokens (bulk copies completing on mbarriers), and each of 8 consumer warps
+// a producer warp streams them through a ring of shared-memory slots of 112
+// tokens (bulk copies completing on mbarriers), and each of 7 consumer warps
 // takes one 16-token tile of every slot and keeps an online softmax per head;
 // the warps' states combine in shared memory, then over the CTAs of a
 // thread-block cluster through distributed shared memory (no global scratch),
@@ -115,9 +115,9 @@ constexpr int kMaxSplit = 8;                     // CTAs per cluster along the t
 
 __device__ uint32_t s_err_kv;
 
-// One ring slot holds 8 consecutive 16-token tiles of one (sequence, KV
+// One ring slot holds 7 consecutive 16-token tiles of one (sequence, KV
 // head): key codes (rows of D * BITS / 8 bytes), value tiles, then ks, vs
-// (fp16) and kz, vz (uint8) per token; each region sized for 8 tiles and
+// (fp16) and kz, vz (uint8) per token; each region sized for 7 tiles and
 // filled from its start (the last slot of a CTA may hold fewer tiles).
 template <int BITS>
 struct KvSlot {
@@ -125,7 +125,7 @@ struct KvSlot {
   static constexpr uint32_t kK = 0, kV = kSlotTiles * kTile, kKs = 2 * kSlotTiles * kTile;
   static constexpr uint32_t kVs = kKs + 32 * kSlotTiles, kKz = kVs + 32 * kSlotTiles, kVz = kKz + 16 * kSlotTiles;
   static constexpr uint32_t kBytes = kVz + 16 * kSlotTiles;
-  static constexpr int kDepth = BITS == 8 ? 3 : 6;  // ~100 KB: two CTAs per SM
+  static constexpr int kDepth = BITS == 8 ? 3 : 6;  // ~90 KB: two CTAs per SM
   static constexpr uint32_t kRing = kDepth * kBytes;
   static constexpr uint32_t kCombine = (uint32_t)(kConsumers + kMaxSplit) * 8 * kState * 4;  // G <= 8
   static constexpr uint32_t kBarOff = kRing > kCombine ? kRing : kCombine;
