@@ -261,6 +261,14 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
+// 2^x on the special-function unit (relative error about 2^-22; results below
+// the normal range flush to zero, and 2^-inf = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -461,10 +469,11 @@ __global__ void __maxnreg__(112) kv_attn_tc_kernel(const AttnParams P) {
       }
       const float mn0 = fmaxf(m0, mt0), mn1 = fmaxf(m1, mt1);  // finite: token t0 is valid
       const bool rescale = !__all_sync(0xffffffffu, mn0 == m0 && mn1 == m1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);  // 0 on the first tile
+      const float al0 = exp2_approx(m0 - mn0), al1 = exp2_approx(m1 - mn1);  // 0 on the first tile
       m0 = mn0;
       m1 = mn1;
-      const float p00 = exp2f(s00 - mn0), p01 = exp2f(s01 - mn1), p10 = exp2f(s10 - mn0), p11 = exp2f(s11 - mn1);
+      const float p00 = exp2_approx(s00 - mn0), p01 = exp2_approx(s01 - mn1), p10 = exp2_approx(s10 - mn0),
+                  p11 = exp2_approx(s11 - mn1);
       l0 = fmaf(l0, al0, p00 + p10);
       l1 = fmaf(l1, al1, p01 + p11);
       // tokens past the length: p = 0, and their (unwritten) scales must not reach P'
