@@ -513,6 +513,23 @@ struct W8TcParams {
   uint32_t bar_off;
 };
 
+// The eight epilogue warps (2..9) only.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// TMA tensor store of a 2-D box from shared memory, as a bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Until the bulk groups have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
 __device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
@@ -521,7 +538,7 @@ __device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (
 template <int BT, bool XH>
 __global__ void __launch_bounds__(kW8TcThreads, 1)
     w8tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                const W8TcParams P) {
+                const __grid_constant__ CUtensorMap tmY, const W8TcParams P) {
   using SH = W8TcShape<BT, XH>;
   constexpr int SC = SH::SC;
   extern __shared__ uint8_t smem_raw[];
@@ -725,29 +742,56 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
   const int row = 32 * q + lane;  // output column within the CTA (TMEM lane)
   constexpr int HALF = BT / 2;    // token columns per epilogue warp
   bool acc_ok = true;
+  // s_x of one tile row and s_w of this thread's column, loaded before the
+  // accumulator is complete so that their latency hides under the last MMAs
+  const int xrow = threadIdx.x - 64;
+  const float sx_mine = epi && xrow < BT && m0 + xrow < P.M ? P.sx[m0 + xrow] : 0.f;
+  const int n_mine = nt0 * 16 + row;
+  const float sw_mine = epi && n_mine < P.N ? P.sw[n_mine] : 0.f;
   if (epi) {
     acc_ok = mbar_wait(bar_acc, 0, abort_flag, &s_err_w8);
     acc_ok = __all_sync(0xffffffffu, acc_ok);
     tc_fence_after();
   }
   if (S == 1) {
-    if (epi) grid_dependency_wait();  // Y may still be read by the preceding grid
+    // The ring is idle once the accumulator is complete (every copy was
+    // consumed by an MMA): the scaled fp16 tile is staged there, rows of 128
+    // columns (256 bytes), with s_x of the tile's rows after it, and leaves
+    // in one TMA tensor store that clips rows past M and columns past N.
+    const uint32_t ystage = base;
+    float* sxs = reinterpret_cast<float*>(smem + BT * 256);
+    if (epi) {
+      if (xrow < BT) sxs[xrow] = sx_mine;  // BT <= 256 epilogue threads
+      epi_sync();
+    }
     if (epi && acc_ok) {
-      const int n = nt0 * 16 + row;
-      const float swn = n < P.N ? P.sw[n] : 0.f;
+      const float swn = sw_mine;
+      // 32 accumulator columns per wait (tcgen05.wait::ld waits for every load in flight)
 #pragma unroll 1
-      for (int c = 0; c < HALF; c += 8) {
-        uint32_t v[8];
-        tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c), v);
-        tc_wait_ld();
-        if (n < P.N) {
+      for (int c = 0; c < HALF; c += 32) {
+        uint32_t v[32];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int m = m0 + h * HALF + c + e;
-            if (m < P.M) P.Y[(size_t)m * P.N + n] = __float2half_rn(__uint_as_float(v[e]) * P.sx[m] * swn);
-          }
+        for (int b = 0; b < 4; ++b)
+          tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c + 8 * b),
+                          *reinterpret_cast<uint32_t(*)[8]>(v + 8 * b));
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int ml = h * HALF + c + e;  // row within the tile
+          sts16(ystage + ml * 256 + row * 2,
+                __half_as_ushort(__float2half_rn(__uint_as_float(v[e]) * sxs[ml] * swn)));
         }
       }
+    }
+    if (epi) {
+      fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
+      epi_sync();
+    }
+    if (warp == 2 && lane == 0 && acc_ok) {
+      grid_dependency_wait();  // Y may still be read by the preceding grid
+      tma_store_2d(&tmY, ystage, nt0 * 16, m0);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the shared memory stays ours until the store has read it
     }
   } else {
     // Split K: every CTA's ring is idle once all of the cluster passes this
@@ -797,8 +841,8 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
 }
 
 template <int BT, bool XH>
-tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8TcParams& P, dim3 grid, int S,
-                        uint32_t smem, cudaStream_t stream) {
+tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const CUtensorMap& tmY, const W8TcParams& P,
+                        dim3 grid, int S, uint32_t smem, cudaStream_t stream) {
   auto kern = w8tc_kernel<BT, XH>;
   static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   if (!smem_attr_once(attr_done, (const void*)kern, (int)kW8SmemMax)) return TM_ERR_CUDA;
@@ -821,7 +865,7 @@ tm_status w8tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmW, const W8
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, tmX, tmW, tmY, P) == cudaSuccess ? TM_OK : TM_ERR_CUDA;
 }
 
 // Shared memory of the tensor-memory kernel: ring, converted X slots, barriers, alignment slack.
@@ -861,6 +905,21 @@ tm_status w8tc_run(const void* xq, const float* sx, const tm_w8_packed* p, void*
   if (S > 1 && (uint32_t)128 * BT * 4 >
                    stages * SH::SLOT + xstages * SH::XF_UNIT + SH::CONV_SLOTS * SH::XF_SLOT)
     return TM_ERR_UNSUPPORTED;
+  // the epilogue stages the fp16 tile and s_x of its rows below the barriers
+  if (S == 1 && (uint32_t)BT * (256 + 4) > stages * SH::SLOT + xstages * SH::XF_UNIT + SH::CONV_SLOTS * SH::XF_SLOT)
+    return TM_ERR_UNSUPPORTED;
+  CUtensorMap tmY;
+  {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return TM_ERR_CUDA;
+    cuuint64_t dims[2] = {(cuuint64_t)p->N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)p->N * 2};
+    cuuint32_t box[2] = {128u, (cuuint32_t)BT};  // 128 output columns x BT rows, 256-byte rows
+    cuuint32_t es[2] = {1, 1};
+    if (fn(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TM_ERR_CUDA;
+  }
   CUtensorMap tmX;
   {
     EncodeTiledFn fn = encode_tiled_fn();
@@ -888,7 +947,7 @@ tm_status w8tc_run(const void* xq, const float* sx, const tm_w8_packed* p, void*
   P.x_off = stages * SH::SLOT;
   P.xf_off = P.x_off + xstages * SH::XF_UNIT;
   P.bar_off = P.xf_off + SH::CONV_SLOTS * SH::XF_SLOT;
-  return w8tc_launch_t<BT, XH>(tmX, p->tm_codes, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem,
+  return w8tc_launch_t<BT, XH>(tmX, p->tm_codes, tmY, P, dim3((unsigned)MB, (unsigned)NB, (unsigned)S), S, smem,
                                stream);
 }
 
