@@ -83,7 +83,8 @@ __device__ __forceinline__ bool tc_wait_time_only(uint32_t bar, uint32_t parity)
 template <int BT, int KU, int SB>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmC,
-              const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ, const TcParams P) {
+              const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmZ,
+              const __grid_constant__ CUtensorMap tmY, const TcParams P) {
   using SH = TcShape<BT, KU, SB>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     acc_ok = __all_sync(0xffffffffu, acc_ok);  // warp-uniform: the epilogue shuffles
     tc_fence_after();
   }
-  if (S == 1) {
+  if (S == 1 && P.silu) {
     if (epi) grid_dependency_wait();  // Y may still be read by the preceding grid
     if (epi && acc_ok) {
       const int n = nt0 * 16 + row;
@@ -321,6 +322,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+    }
+  } else if (S == 1) {
+    // The ring is idle once the accumulator is complete (every copy was
+    // consumed by an MMA): the fp16 tile is staged there, rows of 128
+    // columns (256 bytes), and leaves in one TMA tensor store that clips rows
+    // past M and columns past N.
+    constexpr int CH = HALF < 32 ? HALF : 32;  // accumulator columns per TMEM wait
+    const uint32_t ystage = base;
+    if (epi && acc_ok) {
+#pragma unroll 1
+      for (int c = 0; c < HALF; c += CH) {
+        uint32_t v[CH];
+#pragma unroll
+        for (int b = 0; b < CH / 8; ++b)
+          tc_ld_32x32b_x8(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HALF + c + 8 * b),
+                          *reinterpret_cast<uint32_t(*)[8]>(v + 8 * b));
+        tc_wait_ld();
+#pragma unroll
+        for (int e = 0; e < CH; ++e) {
+          const int ml = h * HALF + c + e;  // row within the tile
+          sts16(ystage + ml * 256 + row * 2, __half_as_ushort(__float2half_rn(__uint_as_float(v[e]))));
+        }
+      }
+    }
+    if (epi) {
+      fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
+      epilogue_sync();
+    }
+    if (warp == 2 && lane == 0 && acc_ok) {
+      grid_dependency_wait();  // Y may still be read by the preceding grid
+      tma_store_2d(&tmY, ystage, nt0 * 16, m0);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the shared memory stays ours until the store has read it
     }
   } else {
     // Split K: every CTA's ring is idle once all of the cluster passes this
@@ -452,8 +486,8 @@ uint32_t tc_smem_request(int device, const TcVariant& v, int stages) {
 }
 
 template <int BT, int KU, int SB>
-tm_status tc_launch_t(const CUtensorMap& tmX, const tm_packed* p, const TcParams& P, int S, uint32_t smem,
-                      cudaStream_t stream) {
+tm_status tc_launch_t(const CUtensorMap& tmX, const CUtensorMap& tmY, const tm_packed* p, const TcParams& P, int S,
+                      uint32_t smem, cudaStream_t stream) {
   auto kern = tc_kernel<BT, KU, SB>;
   static std::atomic<unsigned long long> attr_done{0};  // one bit per device
   if (!smem_attr_once(attr_done, (const void*)kern, (int)kTcSmemMax)) return TM_ERR_CUDA;
@@ -476,7 +510,7 @@ tm_status tc_launch_t(const CUtensorMap& tmX, const tm_packed* p, const TcParams
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, p->tc_codes, p->tc_scales, p->tc_zeros, P);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tmX, p->tc_codes, p->tc_scales, p->tc_zeros, tmY, P);
   return e == cudaSuccess ? TM_OK : TM_ERR_CUDA;
 }
 
@@ -550,6 +584,21 @@ tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return TM_ERR_CUDA;
   }
+  // the output as a tensor for the epilogue's TMA store: 128 columns x BT rows
+  // (the fused silu form writes [M][N/2] with its own stores)
+  CUtensorMap tmY;
+  {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return TM_ERR_CUDA;
+    const int ncols = silu ? L.N / 2 : L.N;
+    cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)ncols * 2};
+    cuuint32_t box[2] = {128u, (cuuint32_t)BT};
+    cuuint32_t es[2] = {1, 1};
+    if (fn(&tmY, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Y, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TM_ERR_CUDA;
+  }
   TcParams P;
   P.Y = reinterpret_cast<__half*>(Y);
   P.M = M;
@@ -565,17 +614,18 @@ tm_status launch_tc(const void* X, const tm_packed* p, void* Y, int M, const tm_
   P.bar_off = tc_bar_off(v, c.stages);
   P.silu = silu ? 1 : 0;
   if (tc_smem_need(v, c.stages) > kTcSmemMax) return TM_ERR_UNSUPPORTED;
+  if ((uint32_t)BT * 256 > v.slot * (uint32_t)c.stages) return TM_ERR_UNSUPPORTED;  // the epilogue's staged tile
   const uint32_t smem = tc_smem_request(p->device, v, c.stages);
   tm_status st = TM_ERR_UNSUPPORTED;
   switch (BT * 16 + v.KU) {
-    case 16 * 16 + 4: st = tc_launch_t<16, 4, 3>(tmX, p, P, S, smem, stream); break;
-    case 32 * 16 + 4: st = tc_launch_t<32, 4, 3>(tmX, p, P, S, smem, stream); break;
-    case 64 * 16 + 4: st = tc_launch_t<64, 4, 3>(tmX, p, P, S, smem, stream); break;
-    case 16 * 16 + 2: st = tc_launch_t<16, 2, 4>(tmX, p, P, S, smem, stream); break;
-    case 32 * 16 + 2: st = tc_launch_t<32, 2, 4>(tmX, p, P, S, smem, stream); break;
-    case 64 * 16 + 2: st = tc_launch_t<64, 2, 4>(tmX, p, P, S, smem, stream); break;
-    case 128 * 16 + 2: st = tc_launch_t<128, 2, 4>(tmX, p, P, S, smem, stream); break;
-    case 256 * 16 + 2: st = tc_launch_t<256, 2, 4>(tmX, p, P, S, smem, stream); break;
+    case 16 * 16 + 4: st = tc_launch_t<16, 4, 3>(tmX, tmY, p, P, S, smem, stream); break;
+    case 32 * 16 + 4: st = tc_launch_t<32, 4, 3>(tmX, tmY, p, P, S, smem, stream); break;
+    case 64 * 16 + 4: st = tc_launch_t<64, 4, 3>(tmX, tmY, p, P, S, smem, stream); break;
+    case 16 * 16 + 2: st = tc_launch_t<16, 2, 4>(tmX, tmY, p, P, S, smem, stream); break;
+    case 32 * 16 + 2: st = tc_launch_t<32, 2, 4>(tmX, tmY, p, P, S, smem, stream); break;
+    case 64 * 16 + 2: st = tc_launch_t<64, 2, 4>(tmX, tmY, p, P, S, smem, stream); break;
+    case 128 * 16 + 2: st = tc_launch_t<128, 2, 4>(tmX, tmY, p, P, S, smem, stream); break;
+    case 256 * 16 + 2: st = tc_launch_t<256, 2, 4>(tmX, tmY, p, P, S, smem, stream); break;
     default: break;
   }
   if (st == TM_OK) set_launch_count(1);

@@ -513,23 +513,6 @@ struct W8TcParams {
   uint32_t bar_off;
 };
 
-// The eight epilogue warps (2..9) only.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-// TMA tensor store of a 2-D box from shared memory, as a bulk group.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Until the bulk groups have read their shared-memory sources.
-__device__ __forceinline__ void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
 __device__ __forceinline__ void tc_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
@@ -762,7 +745,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
     float* sxs = reinterpret_cast<float*>(smem + BT * 256);
     if (epi) {
       if (xrow < BT) sxs[xrow] = sx_mine;  // BT <= 256 epilogue threads
-      epi_sync();
+      epilogue_sync();
     }
     if (epi && acc_ok) {
       const float swn = sw_mine;
@@ -785,7 +768,7 @@ __global__ void __launch_bounds__(kW8TcThreads, 1)
     }
     if (epi) {
       fence_proxy_async_smem();  // the staged tile is read by the TMA (async proxy)
-      epi_sync();
+      epilogue_sync();
     }
     if (warp == 2 && lane == 0 && acc_ok) {
       grid_dependency_wait();  // Y may still be read by the preceding grid
