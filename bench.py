@@ -263,16 +263,33 @@ class Workload:
         self.step_flops = sum(i["flops"] for i in self.items)
         self.weight_bytes = sum(i["w"].nbytes for i in self.items)
 
-    def launch_all(self, stream, events=None):
+    def runs(self):
+        """The step's products as launches: consecutive products with the same
+        M <= 32 (the four linears of a layer at one batch size) share one
+        grouped launch; every other product is a launch of its own."""
+        from w4a16_quantized_gemm_gb300 import binding
+        out = []
+        for it in self.items:
+            M = it["case"].M
+            last = out[-1] if out else None
+            if (last and M <= 32 and last[0]["case"].M == M and last[0]["case"].g == it["case"].g
+                    and len(last) < binding.GROUP_MAX):
+                last.append(it)
+            else:
+                out.append([it])
+        return out
+
+    def launch_all(self, stream, grouped=True):
+        """One step: the grouped launches of runs() (grouped=False: every
+        product launched on its own).  Returns the number of kernel launches."""
         from w4a16_quantized_gemm_gb300 import binding
         n = 0
-        for k, it in enumerate(self.items):
-            if events is not None:
-                events[k].record(stream)
-            binding.gemm(it["X"], it["w"], out=it["Y"], stream=stream)
+        for run in (self.runs() if grouped else [[it] for it in self.items]):
+            if len(run) > 1:
+                binding.gemm_grouped([(it["X"], it["w"], it["Y"], False) for it in run], stream=stream)
+            else:
+                binding.gemm(run[0]["X"], run[0]["w"], out=run[0]["Y"], stream=stream)
             n += binding.last_launch_count()
-        if events is not None:
-            events[len(self.items)].record(stream)
         return n
 
 
@@ -368,8 +385,11 @@ def run_gpu(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(t_max_s * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": workload_config(args.workload, world),
-        "launch": f"one CUDA graph per step ({len(wl.items)} kernel nodes, programmatic dependent launch); "
-                  f"{wl.weight_bytes} bytes of distinct packed weights per step; fp32 accumulation",
+        "launch": f"one CUDA graph per step ({launches_per_step} kernel nodes for {len(wl.items)} products, "
+                  f"programmatic dependent launch"
+                  + ("; the products of one M (a layer's four linears, independent inputs) share one grouped "
+                     "launch, tm_w4a16_gemm_grouped" if launches_per_step < len(wl.items) else "")
+                  + f"); {wl.weight_bytes} bytes of distinct packed weights per step; fp32 accumulation",
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
                      "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peaks["source"],
@@ -377,7 +397,8 @@ def run_gpu(args, rank, world, local):
                      "basis": "algorithmic units of the step's launches / mean step time of the timed "
                               "region (CUDA events around each graph replay); consecutive launches overlap "
                               "under programmatic dependent launch, so the step time is their combined "
-                              "duration and the average launch duration is step time / launches"},
+                              "duration and the average launch duration is step time / launches",
+                     "launches_per_step": launches_per_step},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "e2e": e2e,
@@ -430,10 +451,11 @@ def _pack_copies(key, device, min_bytes):
     return copies, sal
 
 
-def _decode_step_at_m(wl, M, stream, peaks, rounds=3):
+def _decode_step_at_m(wl, M, stream, peaks, rounds=3, grouped=False):
     """The four Llama-3-8B layers of the headline workload at one M (qkv,
-    o_proj, gate_up, down: one decoder layer's linears at batch M), launched in
-    order on `rounds` distinct copies of their weights (> L2 together)."""
+    o_proj, gate_up, down: one decoder layer's linears at batch M), on
+    `rounds` distinct copies of their weights (> L2 together): launched one by
+    one in order, or (grouped) as one grouped launch per copy."""
     from w4a16_quantized_gemm_gb300 import binding
     items = [it for it in wl.items if it["case"].M == M]
     sets = [[it["w"] for it in items]]
@@ -446,17 +468,25 @@ def _decode_step_at_m(wl, M, stream, peaks, rounds=3):
 
     def launch(st):
         for ws in sets:
-            for it, w in zip(items, ws):
-                binding.gemm(it["X"], w, out=it["Y"], stream=st)
+            if grouped:
+                binding.gemm_grouped([(it["X"], w, it["Y"], False) for it, w in zip(items, ws)], stream=st)
+            else:
+                for it, w in zip(items, ws):
+                    binding.gemm(it["X"], w, out=it["Y"], stream=st)
     ms = _time_graph(launch, stream, 10) / rounds
+    plan = binding.plan_grouped(sets[0], M) if grouped else None
     for ws in sets[1:]:
         for w in ws:
             w.free()
     nbytes = sum(it["bytes"] for it in items)
     nflops = sum(it["flops"] for it in items)
-    return {"config": 1, "step": f"llama3-8b layer linears at M={M}", "M": M, "us": round(ms * 1e3, 2),
-            "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes,
-            "roofline": roofline_entry(nbytes, nflops, ms * 1e-3, peaks)}
+    how = "one grouped launch" if grouped else "four launches"
+    e = {"config": 1, "step": f"llama3-8b layer linears at M={M}, {how}", "M": M, "grouped": grouped,
+         "us": round(ms * 1e3, 2), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes,
+         "roofline": roofline_entry(nbytes, nflops, ms * 1e-3, peaks)}
+    if plan:
+        e["plan"] = plan
+    return e
 
 
 def _decode_step_concurrent(wl, stream, peaks, rounds=3):
@@ -555,14 +585,21 @@ def config_detail(wl, stream, peaks, args, min_bytes=300e6, reps=5):
         del copies
         torch.cuda.empty_cache()
     dwl = wl if wl.kind == "decode" else Workload("decode", device)  # the step figures are the decode workload's
-    steps = [_decode_step_at_m(dwl, M, stream, peaks) for M in (1, 8, 16, 32)]
-    out.extend(steps)
-    small = [e for e in steps if e["M"] <= 16]
-    nb = sum(e["bytes"] for e in small)
-    t = sum(e["us"] for e in small) * 1e-6
-    out.append({"config": 1, "step": "llama3-8b layer linears at M in {1,8,16} (the decode target's range)",
-                "us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
-                "roofline": roofline_entry(nb, 0, t, peaks)})
+    for grouped in (True, False):
+        steps = [_decode_step_at_m(dwl, M, stream, peaks, grouped=grouped) for M in (1, 8, 16, 32)]
+        out.extend(steps)
+        small = [e for e in steps if e["M"] <= 16]
+        nb = sum(e["bytes"] for e in small)
+        t = sum(e["us"] for e in small) * 1e-6
+        how = "one grouped launch per M" if grouped else "one launch per GEMM"
+        out.append({"config": 1, "step": f"llama3-8b layer linears at M in {{1,8,16}} (the decode target's range), "
+                                         f"{how}", "grouped": grouped,
+                    "us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
+                    "roofline": roofline_entry(nb, 0, t, peaks)})
+    ms = _time_graph(lambda st: dwl.launch_all(st, grouped=False), stream, 20)
+    out.append({"config": 1, "step": "llama3-8b decode step, the 16 GEMMs launched one by one (16 launches)",
+                "us": round(ms * 1e3, 2), "GB/s": round(dwl.step_bytes / (ms * 1e-3) / 1e9, 1),
+                "roofline": roofline_entry(dwl.step_bytes, dwl.step_flops, ms * 1e-3, peaks)})
     out.append(_decode_step_concurrent(dwl, stream, peaks))
     out.append(_prefill_step(device, stream, peaks, max(5, min(args.steps, 50))))
     return out
@@ -593,6 +630,10 @@ def run_e2e(wl, args, spec):
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
 
     batches[0].run(streams[0])  # waits for the stream
+    # the device-resident step's own launches, now (the detail figures rewrite Y with other settings)
+    with torch.cuda.stream(streams[1]):
+        wl.launch_all(streams[1])
+    streams[1].synchronize()
     same = all(torch.equal(batches[0].y(i).view(torch.int16), it["Y"].cpu().view(torch.int16))
                for i, it in enumerate(wl.items))
 

@@ -219,6 +219,57 @@ tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, int M, void*
 tm_status tm_w4a16_gemm_silu_mul(const void* X, const tm_packed* p, void* H, int M, const tm_gemm_config* cfg,
                                  void* stream);
 
+/* Most products one tm_w4a16_gemm_grouped call puts in one launch. */
+#define TM_GROUP_MAX 4
+
+/* One product of tm_w4a16_gemm_grouped. */
+typedef struct {
+  const void* X;      /* device fp16 [M][K] row-major, 16-byte aligned (K: the handle's) */
+  const tm_packed* p; /* packed weights, K x N */
+  void* Y;            /* device fp16 [M][N] (silu: [M][N/2]) row-major, 16-byte aligned, written in full */
+  int silu;           /* 0: Y = X . W;  1: Y = silu(X . W_gate) * (X . W_up) as tm_w4a16_gemm_silu_mul */
+} tm_gemm_problem;
+
+/*
+ * n independent products of the same M in ONE kernel launch (the decode
+ * kernel, M <= 32): the launch's CTAs cover the column blocks of all n
+ * products, so the weight stream of one product runs on while another's
+ * last CTAs reduce and store, and the launch's start-up and tail are paid
+ * once instead of n times.  The products are those of tm_w4a16_gemm /
+ * tm_w4a16_gemm_silu_mul, bit for bit equal to them under the same launch
+ * settings (tile_n, warp_n and the product's split as split_k: see
+ * tm_gemm_plan_grouped).  The paper
+ * has no counterpart to this call; it is a property of this library.
+ *
+ *   probs: host array of n products, 1 <= n <= TM_GROUP_MAX; every handle on
+ *          the current device, all with the same group size g (K and N may
+ *          differ).  No product may read what another writes: every Y must
+ *          be disjoint from every X and from every other Y (checked on the
+ *          address ranges: TM_ERR_INVALID_ARG).
+ *   cfg:   NULL = automatic, else path 0 or 1 and the decode fields, applied
+ *          to every product: tile_n 64 or 128, warp_n 0 or 1, stages, and
+ *          split_k (every product split that many ways; automatic: each
+ *          product split by its own K, see tm_gemm_plan_grouped).
+ * M > 32 with automatic settings runs the n products one after another, as n
+ * tm_w4a16_gemm calls would (n launches).  Asynchronous on `stream`; no
+ * allocation.  M == 0 is a no-op.  Errors: TM_ERR_INVALID_ARG (NULL pointer,
+ * n out of range, mixed group sizes, overlapping buffers, silu with
+ * N % 8 != 0), TM_ERR_ALIGNMENT, TM_ERR_UNSUPPORTED (settings the decode
+ * kernel does not serve), TM_ERR_CUDA.  tm_last_launch_count reports the
+ * launches made.
+ */
+tm_status tm_w4a16_gemm_grouped(const tm_gemm_problem* probs, int n, int M, const tm_gemm_config* cfg, void* stream);
+
+/* The settings tm_w4a16_gemm_grouped would use (all fields of *out filled
+ * in; out->split_k is the cluster size of the launch) and, when `splits` is
+ * not NULL, each product's split along K (splits[i], a power of two dividing
+ * out->split_k; automatic settings split each product by its own K).  Only
+ * X, p and silu of each problem are read.  With M > 32 and automatic
+ * settings, *out is the first product's own plan and splits[i] each
+ * product's own split. */
+tm_status tm_gemm_plan_grouped(const tm_gemm_problem* probs, int n, int M, const tm_gemm_config* cfg,
+                               tm_gemm_config* out, int* splits);
+
 /* tm_w4a16_gemm with explicit launch settings (cfg may be NULL = automatic). */
 tm_status tm_w4a16_gemm_ex(const void* X, const tm_packed* p, void* Y, int M, const tm_gemm_config* cfg,
                            void* stream);
@@ -249,10 +300,13 @@ tm_status tm_w4a16_gemm_host(const void* X_host, const tm_packed* p, void* Y_hos
  *   sum M[i] N_i fp16, 16-byte aligned; every X_i and Y_i then starts on a
  *   32-byte boundary (K_i % 64 == 0, N_i % 16 == 0).
  * On `stream`: one host-to-device copy, the n products in order (automatic
- * plans, as tm_w4a16_gemm), one device-to-host copy; asynchronous, the caller
- * synchronises before reading Y_host.  Every product is planned before the
- * first copy: a rejected argument leaves all buffers untouched.  M[i] == 0
- * skips product i.  tm_last_launch_count reports the kernels of all n.
+ * plans), one device-to-host copy; asynchronous, the caller synchronises
+ * before reading Y_host.  Consecutive products with the same M <= 32 and the
+ * same g, up to TM_GROUP_MAX of them, share one launch as in
+ * tm_w4a16_gemm_grouped (automatic settings); every other product runs as
+ * tm_w4a16_gemm.  Every product is planned before the first copy: a rejected
+ * argument leaves all buffers untouched.  M[i] == 0 skips product i.
+ * tm_last_launch_count reports the kernels of all n.
  */
 tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, const int* M, const void* X_host, void* Y_host,
                                    void* X_dev, void* Y_dev, void* stream);

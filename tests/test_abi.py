@@ -84,6 +84,22 @@ def test_null_arguments_are_rejected(lib):
     assert lib.tm_last_launch_count() == 0
 
 
+def test_grouped_entry_points_reject_bad_host_arguments(lib):
+    """tm_w4a16_gemm_grouped / tm_gemm_plan_grouped check the problem list on
+    the host before touching a handle (no device needed)."""
+    from w4a16_quantized_gemm_gb300 import binding
+    out = binding.GemmConfig()
+    arr = (binding.GemmProblem * (binding.GROUP_MAX + 1))()
+    assert lib.tm_w4a16_gemm_grouped(None, 1, 1, None, None) == 1
+    assert lib.tm_w4a16_gemm_grouped(arr, 0, 1, None, None) == 1
+    assert lib.tm_w4a16_gemm_grouped(arr, binding.GROUP_MAX + 1, 1, None, None) == 1
+    assert lib.tm_w4a16_gemm_grouped(arr, 1, 1, None, None) == 1          # NULL handle
+    assert lib.tm_w4a16_gemm_grouped(arr, 1, -1, None, None) == 1
+    assert lib.tm_gemm_plan_grouped(arr, 1, 1, None, None, None) == 1     # NULL out
+    assert lib.tm_gemm_plan_grouped(None, 1, 1, None, ctypes.byref(out), None) == 1
+    assert lib.tm_last_launch_count() == 0
+
+
 def test_library_has_sm103a_code():
     """The build targets sm_103a only (checked from the build flags)."""
     from w4a16_quantized_gemm_gb300 import build

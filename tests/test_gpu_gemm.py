@@ -247,6 +247,32 @@ def test_gemm_host_batch_matches_oracle_every_product():
     assert binding.device_error(clear=True) == 0
 
 
+def test_gemm_host_batch_groups_runs_of_the_same_m():
+    """Consecutive products with the same M <= 32 and group size share one
+    grouped launch (three g = 128, then, after an M = 0 product, two g = 64);
+    M = 40 runs on its own: three launches, every product against the oracle."""
+    import oracle
+    shapes = [(3, 1024, 384, 128), (3, 512, 256, 128), (3, 2048, 1040, 128), (0, 512, 256, 64),
+              (3, 1024, 2048, 64), (3, 4096, 512, 64), (40, 512, 2048, 128)]
+    ws = [packed(K, N, g, seed=10 + i) for i, (M, K, N, g) in enumerate(shapes)]
+    batch = binding.HostBatch(ws, [sh[0] for sh in shapes])
+    Xs = []
+    for i, (M, K, N, g) in enumerate(shapes):
+        X = activations(M, K, N, g, seed=10 + i)
+        Xs.append(X)
+        batch.x(i).copy_(torch.from_numpy(X.view(np.uint16)).view(torch.float16))
+    batch.Y_host.fill_(float("nan"))
+    batch.run()
+    assert binding.last_launch_count() == 3
+    for i, (M, K, N, g) in enumerate(shapes):
+        if M == 0:
+            continue
+        q, z, s, _ = host_weights(K, N, g, seed=10 + i)
+        err = oracle.rel_max_err(batch.y(i).float().numpy().astype(np.float64), oracle.gemm(Xs[i], q, z, s, g))
+        assert err <= TOL, (i, err)
+    assert binding.device_error(clear=True) == 0
+
+
 def test_one_launch_per_call():
     w = packed(1024, 384, 128)
     X = torch.zeros((4, 1024), dtype=torch.float16, device="cuda")

@@ -26,7 +26,10 @@ EXPORTS = ("tm_status_str", "tm_packed_bytes", "tm_pack_weights", "tm_unpack_wei
            "tm_kv_quantize", "tm_kv_decode_attention", "tm_kv_pack_v", "tm_w8a8_quantize_act", "tm_w8_pack",
            "tm_w8_unpack", "tm_w8_packed_info", "tm_w8_packed_free", "tm_w8a8_gemm", "tm_w8a8_gemm_ex",
            "tm_w8_quantize_weight", "tm_kv_append", "tm_w4a16_gemm_host", "tm_w4a16_gemm_host_batch",
-           "tm_w8a8_quantize_act_f16", "tm_w8a8_gemm_f16", "tm_w4a16_gemm_host_static")
+           "tm_w8a8_quantize_act_f16", "tm_w8a8_gemm_f16", "tm_w4a16_gemm_host_static",
+           "tm_w4a16_gemm_grouped", "tm_gemm_plan_grouped")
+
+GROUP_MAX = 4  # TM_GROUP_MAX
 
 
 class TMError(RuntimeError):
@@ -41,6 +44,10 @@ class GemmConfig(ctypes.Structure):
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class GemmProblem(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("p", ctypes.c_void_p), ("Y", ctypes.c_void_p), ("silu", ctypes.c_int)]
 
 
 _lib = None
@@ -124,6 +131,9 @@ def load(path: Optional[str] = None):
     lib.tm_w8a8_quantize_act_f16.argtypes = [vp, ci, ci, vp, vp, vp]
     lib.tm_w8a8_gemm_f16.restype = ci
     lib.tm_w8a8_gemm_f16.argtypes = [vp, vp, vp, vp, ci, ci, ci, vp]
+    lib.tm_w4a16_gemm_grouped.argtypes = [ctypes.POINTER(GemmProblem), ci, ci, ctypes.POINTER(GemmConfig), vp]
+    lib.tm_gemm_plan_grouped.argtypes = [ctypes.POINTER(GemmProblem), ci, ci, ctypes.POINTER(GemmConfig),
+                                         ctypes.POINTER(GemmConfig), ctypes.POINTER(ci)]
     _lib = lib
     return lib
 
@@ -270,6 +280,64 @@ def gemm_silu_mul(X: torch.Tensor, w: PackedWeights, out: Optional[torch.Tensor]
                                          ctypes.byref(c) if c else None, ctypes.c_void_p(s.cuda_stream)),
            "tm_w4a16_gemm_silu_mul")
     return out
+
+
+def _problems(items, M, check_out=True):
+    arr = (GemmProblem * len(items))()
+    for i, (X, w, out, silu) in enumerate(items):
+        arr[i].X = X.data_ptr() if X is not None else None
+        arr[i].p = w.handle
+        arr[i].Y = out.data_ptr() if out is not None else None
+        arr[i].silu = 1 if silu else 0
+    return arr
+
+
+def plan_grouped(weights, M: int, config=None, silu=None) -> dict:
+    """Settings tm_w4a16_gemm_grouped would use for these packed weights at M
+    rows; "splits" lists each product's split along K ("split_k" is the
+    launch's cluster size)."""
+    silu = list(silu) if silu is not None else [False] * len(weights)
+    arr = _problems([(None, w, None, f) for w, f in zip(weights, silu)], M)
+    out = GemmConfig()
+    splits = (ctypes.c_int * max(1, len(weights)))()
+    c = _cfg(config)
+    _check(load().tm_gemm_plan_grouped(arr, len(weights), M, ctypes.byref(c) if c else None, ctypes.byref(out),
+                                       splits), "tm_gemm_plan_grouped")
+    d = out.as_dict()
+    d["splits"] = [splits[i] for i in range(len(weights))]
+    return d
+
+
+def gemm_grouped(problems, config=None, stream: Optional[torch.cuda.Stream] = None):
+    """Independent products of the same M in one launch (tm_w4a16_gemm_grouped).
+
+    problems: up to GROUP_MAX tuples (X, w, out, silu) -- X CUDA fp16 [M][K],
+    w PackedWeights, out a CUDA fp16 [M][N] tensor ([M][N/2] with silu) or
+    None to allocate, silu a bool.  No out may overlap any X or another out.
+    Returns the list of outputs; asynchronous on ``stream``."""
+    items = []
+    M = None
+    for X, w, out, silu in problems:
+        if X.dim() != 2 or X.shape[1] != w.K or X.dtype != torch.float16 or not X.is_cuda:
+            raise ValueError("every X must be a CUDA fp16 [M][K] tensor")
+        if M is None:
+            M = X.shape[0]
+        elif X.shape[0] != M:
+            raise ValueError("every X must have the same number of rows")
+        cols = w.N // 2 if silu else w.N
+        if out is None:
+            out = torch.empty((M, cols), dtype=torch.float16, device=X.device)
+        elif out.shape != (M, cols) or out.dtype != torch.float16 or not out.is_cuda or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous CUDA fp16 [{M}][{cols}] tensor")
+        items.append((X.contiguous(), w, out, bool(silu)))
+    if not items:
+        raise ValueError("at least one problem")
+    s = stream if stream is not None else torch.cuda.current_stream(items[0][0].device)
+    c = _cfg(config)
+    arr = _problems(items, M)
+    _check(load().tm_w4a16_gemm_grouped(arr, len(items), M, ctypes.byref(c) if c else None,
+                                        ctypes.c_void_p(s.cuda_stream)), "tm_w4a16_gemm_grouped")
+    return [it[2] for it in items]
 
 
 def _gemm_host(X, w, out, config, stream):

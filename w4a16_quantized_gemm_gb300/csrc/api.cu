@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "decode_group.h"
 #include "tm_common.cuh"
 
 namespace w4 {
@@ -176,6 +177,103 @@ extern "C" tm_status tm_w4a16_gemm(const void* X, const tm_packed* p, void* Y, i
   return tm_w4a16_gemm_ex(X, p, Y, M, nullptr, stream);
 }
 
+namespace {
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Checks of tm_w4a16_gemm_grouped's arguments; on TM_OK fills jobs and ps.
+tm_status check_group(const tm_gemm_problem* probs, int n, int M, DecodeJob* jobs, const tm_packed** ps) {
+  if (!probs || n < 1 || n > TM_GROUP_MAX || M < 0) return TM_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    const tm_gemm_problem& q = probs[i];
+    if (!q.p || (M > 0 && (!q.X || !q.Y))) return TM_ERR_INVALID_ARG;
+    if (q.p->L.g != probs[0].p->L.g || q.p->device != probs[0].p->device) return TM_ERR_INVALID_ARG;
+    if (q.silu && q.p->L.N % 8 != 0) return TM_ERR_INVALID_ARG;
+    jobs[i] = {q.X, q.p, q.Y, q.silu != 0};
+    ps[i] = q.p;
+  }
+  if (M == 0) return TM_OK;
+  for (int i = 0; i < n; ++i) {
+    if (!aligned16(probs[i].X) || !aligned16(probs[i].Y)) return TM_ERR_ALIGNMENT;
+    const size_t yb = (size_t)M * (probs[i].silu ? probs[i].p->L.N / 2 : probs[i].p->L.N) * 2;
+    for (int j = 0; j < n; ++j) {
+      const size_t xb = (size_t)M * probs[j].p->L.K * 2;
+      if (ranges_overlap(probs[i].Y, yb, probs[j].X, xb)) return TM_ERR_INVALID_ARG;
+      if (j != i) {
+        const size_t yb2 = (size_t)M * (probs[j].silu ? probs[j].p->L.N / 2 : probs[j].p->L.N) * 2;
+        if (ranges_overlap(probs[i].Y, yb, probs[j].Y, yb2)) return TM_ERR_INVALID_ARG;
+      }
+    }
+  }
+  return TM_OK;
+}
+
+// Grouped launch when the path is the decode kernel (explicit path 1, or
+// automatic with M <= 32); *grouped = false means one launch per product.
+tm_status plan_group(const tm_packed* const* ps, int n, int M, const tm_gemm_config* cfg, tm_gemm_config* out,
+                     int* splits, bool* grouped) {
+  const int path = cfg ? cfg->path : 0;
+  if (path != 0 && path != 1) return TM_ERR_INVALID_ARG;
+  *grouped = path == 1 || M <= kAutoDecodeMaxM;
+  if (!*grouped) return TM_OK;
+  if (M > kDecodeMaxM) return TM_ERR_UNSUPPORTED;
+  return plan_decode_group(ps, n, M > 0 ? M : 1, cfg, out, splits);
+}
+
+}  // namespace
+
+extern "C" tm_status tm_gemm_plan_grouped(const tm_gemm_problem* probs, int n, int M, const tm_gemm_config* cfg,
+                                          tm_gemm_config* out, int* splits) {
+  DecodeJob jobs[TM_GROUP_MAX];
+  const tm_packed* ps[TM_GROUP_MAX];
+  if (!out) return TM_ERR_INVALID_ARG;
+  tm_status st = check_group(probs, n, 0, jobs, ps);
+  if (st != TM_OK) return st;
+  bool grouped = false;
+  st = plan_group(ps, n, M, cfg, out, splits, &grouped);
+  if (st != TM_OK || grouped) return st;
+  // One launch per product: each product's own automatic settings.
+  for (int i = n - 1; i >= 0; --i) {
+    st = plan(ps[i], M, nullptr, out);
+    if (st != TM_OK) return st;
+    if (splits) splits[i] = out->split_k;
+  }
+  return TM_OK;
+}
+
+extern "C" tm_status tm_w4a16_gemm_grouped(const tm_gemm_problem* probs, int n, int M, const tm_gemm_config* cfg,
+                                           void* stream) {
+  t_launches = 0;
+  DecodeJob jobs[TM_GROUP_MAX];
+  const tm_packed* ps[TM_GROUP_MAX];
+  tm_status st = check_group(probs, n, M, jobs, ps);
+  if (st != TM_OK || M == 0) return st;
+  tm_gemm_config c;
+  bool grouped = false;
+  st = plan_group(ps, n, M, cfg, &c, nullptr, &grouped);
+  if (st != TM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (grouped) return launch_decode_group(jobs, n, M, cfg, s);
+  // Every product is planned before the first launch.
+  tm_gemm_config cs[TM_GROUP_MAX];
+  for (int i = 0; i < n; ++i) {
+    st = plan(ps[i], M, nullptr, &cs[i]);
+    if (st != TM_OK) return st;
+  }
+  int launches = 0;
+  for (int i = 0; i < n; ++i) {
+    st = probs[i].silu ? tm_w4a16_gemm_silu_mul(probs[i].X, ps[i], probs[i].Y, M, &cs[i], stream)
+                       : tm_w4a16_gemm_ex(probs[i].X, ps[i], probs[i].Y, M, &cs[i], stream);
+    if (st != TM_OK) return st;
+    launches += t_launches;
+  }
+  t_launches = launches;
+  return TM_OK;
+}
+
 extern "C" tm_status tm_w4a16_gemm_host(const void* X_host, const tm_packed* p, void* Y_host, int M, void* X_dev,
                                         void* Y_dev, const tm_gemm_config* cfg, void* stream) {
   t_launches = 0;
@@ -211,18 +309,46 @@ extern "C" tm_status tm_w4a16_gemm_host_batch(int n, const tm_packed* const* p, 
   if (xb == 0) return TM_OK;
   if (!X_host || !Y_host || !X_dev || !Y_dev) return TM_ERR_INVALID_ARG;
   if (!aligned16(X_dev) || !aligned16(Y_dev)) return TM_ERR_ALIGNMENT;
+  // Runs of consecutive products with the same M <= 32 and group size (at
+  // most TM_GROUP_MAX) share one grouped launch: their staging regions are
+  // disjoint, so the products are independent.
+  auto run_end = [&](int i) {
+    int j = i + 1;
+    if (M[i] > kAutoDecodeMaxM) return j;
+    while (j < n && j - i < TM_GROUP_MAX && M[j] == M[i] && p[j]->L.g == p[i]->L.g && p[j]->device == p[i]->device)
+      ++j;
+    return j;
+  };
+  for (int i = 0; i < n;) {
+    const int j = M[i] > 0 ? run_end(i) : i + 1;
+    if (j - i > 1) {
+      tm_gemm_config c;
+      const tm_status st = plan_decode_group(p + i, j - i, M[i], nullptr, &c, nullptr);
+      if (st != TM_OK) return st;
+    }
+    i = j;
+  }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemcpyAsync(X_dev, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return TM_ERR_CUDA;
   size_t xo = 0, yo = 0;
   int launches = 0;
-  for (int i = 0; i < n; ++i) {
-    if (M[i] == 0) continue;
-    const tm_status st = tm_w4a16_gemm_ex(static_cast<const char*>(X_dev) + xo, p[i],
-                                          static_cast<char*>(Y_dev) + yo, M[i], nullptr, stream);
+  for (int i = 0; i < n;) {
+    if (M[i] == 0) {
+      ++i;
+      continue;
+    }
+    const int j = run_end(i);
+    DecodeJob jobs[TM_GROUP_MAX];
+    for (int k = i; k < j; ++k) {
+      jobs[k - i] = {static_cast<const char*>(X_dev) + xo, p[k], static_cast<char*>(Y_dev) + yo, false};
+      xo += (size_t)M[k] * p[k]->L.K * 2;
+      yo += (size_t)M[k] * p[k]->L.N * 2;
+    }
+    const tm_status st = j - i > 1 ? launch_decode_group(jobs, j - i, M[i], nullptr, s)
+                                   : tm_w4a16_gemm_ex(jobs[0].X, p[i], jobs[0].Y, M[i], nullptr, stream);
     if (st != TM_OK) return st;
     launches += t_launches;
-    xo += (size_t)M[i] * p[i]->L.K * 2;
-    yo += (size_t)M[i] * p[i]->L.N * 2;
+    i = j;
   }
   if (cudaMemcpyAsync(Y_host, Y_dev, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess) return TM_ERR_CUDA;
   t_launches = launches;
