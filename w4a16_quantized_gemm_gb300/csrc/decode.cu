@@ -101,7 +101,8 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_kernel(const __grid_cons
   constexpr int CNN = CN * 16;   // columns per CTA
   constexpr int UPG = UPS / 2;   // units (of 64 k) per group
   constexpr int NACC = 1;  // accumulator chains per tile (more measured slower)
-  // Raw-code products pay off when the all-ones product is shared by several tiles.
+  // Raw-code products pay off when the all-ones product is shared by several
+  // tiles (with one tile per warp they measured slower, single or grouped).
   constexpr bool kRaw = WN >= 2 && MT < 4 * WN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_u32(smem_raw);
@@ -611,7 +612,9 @@ tm_status launch_u(int UPS, const DecodeMaps<G>& maps, const DecodeParams<G>& P,
 }
 
 // Served CTA shapes: WN 1 with 4 or 8 warps; for a single product also WN 2
-// with 4 or 8 warps (M <= 32) and WN 4 with 2 or 4 warps (M <= 16).
+// with 4 or 8 warps (M <= 32) and WN 4 with 2 or 4 warps (M <= 16).  (Two
+// tiles a warp in a grouped launch measured slower: 32.3 against 26.8 us
+// for the 8B layer at M = 1.)
 template <int MT, bool XP, int G>
 tm_status launch_m(int WN, int NW, int UPS, const DecodeMaps<G>& maps, const DecodeParams<G>& P, int blocks, int C,
                    uint32_t smem, cudaStream_t stream, const void** query) {
@@ -646,17 +649,17 @@ tm_status dispatch(int MT, bool XP, int WN, int NW, int UPS, const DecodeMaps<G>
 // Resident CTAs per SM that the registers and threads of the grouped
 // instantiation allow (occupancy calculator at a small shared-memory
 // request), cached per instantiation.
-int group_ctas_by_registers(int MT, bool XP, int NW, int UPS) {
+int group_ctas_by_registers(int MT, bool XP, int WN, int NW, int UPS) {
   static std::mutex mu;
-  static int cache[4][2][2][2] = {};  // MT index, XP, NW 4/8, UPS 2/4
+  static int cache[4][2][2][2][2] = {};  // MT index, XP, WN 1/2, NW 4/8, UPS 2/4
   const int mi = MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lk(mu);
-  int& c = cache[mi][XP ? 1 : 0][NW == 8 ? 1 : 0][UPS == 4 ? 1 : 0];
+  int& c = cache[mi][XP ? 1 : 0][WN == 2 ? 1 : 0][NW == 8 ? 1 : 0][UPS == 4 ? 1 : 0];
   if (c) return c;
   const void* k = nullptr;
   const DecodeMaps<kGroupMax> maps = {};
   const DecodeParams<kGroupMax> P = {};
-  if (dispatch<kGroupMax>(MT, XP, 1, NW, UPS, maps, P, 1, 1, 0, nullptr, &k) != TM_OK || !k) return 1;
+  if (dispatch<kGroupMax>(MT, XP, WN, NW, UPS, maps, P, 1, 1, 0, nullptr, &k) != TM_OK || !k) return 1;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, (NW + 1) * 32, 4096) != cudaSuccess || n < 1) n = 1;
   c = n;
@@ -851,8 +854,9 @@ tm_status plan_decode_group(const tm_packed* const* ps, int n, int M, const tm_g
   if (want_stages && (want_stages < 2 || want_stages > 8)) return TM_ERR_INVALID_ARG;
   if (want_wn && want_wn != 1) return TM_ERR_UNSUPPORTED;
   const int tile = want_tile ? want_tile : 64;
+  const int wn = 1;
   int WN = 0, NW = 0;
-  if (!tile_shape(tile, 1, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
+  if (!tile_shape(tile, wn, MT, &WN, &NW)) return TM_ERR_UNSUPPORTED;
   const int CN = WN * NW;
   int sp[kGroupMax];
   int C = 1;
@@ -873,7 +877,7 @@ tm_status plan_decode_group(const tm_packed* const* ps, int n, int M, const tm_g
     int per_sm = 0, reserved = 0;
     sm_shared_memory(ps[0]->device, &per_sm, &reserved);
     const int sms = num_sms(ps[0]->device);
-    const int r = std::max(1, std::min((ctas + sms - 1) / sms, group_ctas_by_registers(MT, g.xp, NW, ps[0]->L.UPS)));
+    const int r = std::max(1, std::min((ctas + sms - 1) / sms, group_ctas_by_registers(MT, g.xp, WN, NW, ps[0]->L.UPS)));
     const uint32_t budget = std::min<uint32_t>((uint32_t)std::max(0, per_sm / r - reserved), kSmemPerCta);
     stages = std::min(std::max(2, per_cta), std::max(2, fit_stages(g, budget)));
     // At most 8 CTAs an SM: a 1-row launch with 2 stages fits 9, and when a
@@ -886,7 +890,7 @@ tm_status plan_decode_group(const tm_packed* const* ps, int n, int M, const tm_g
       ++stages;
   }
   if (smem_bytes(g, stages) > kSmemPerCta) return TM_ERR_UNSUPPORTED;
-  *out = {1, C, tile, stages, 1, 0};
+  *out = {1, C, tile, stages, wn, 0};
   if (splits)
     for (int i = 0; i < n; ++i) splits[i] = sp[i];
   return TM_OK;
