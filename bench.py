@@ -279,17 +279,39 @@ class Workload:
                 out.append([it])
         return out
 
-    def launch_all(self, stream, grouped=True):
+    def launch_all(self, stream, grouped=True, concurrent=True):
         """One step: the grouped launches of runs() (grouped=False: every
-        product launched on its own).  Returns the number of kernel launches."""
+        product launched on its own).  In the prefill workload (concurrent)
+        the M = 128 products, bound by their weight stream, run on a second
+        stream beside the tensor-bound ones (those largest first), joined
+        before the step ends; the products are independent.  Returns the
+        number of kernel launches."""
+        import torch
+
         from w4a16_quantized_gemm_gb300 import binding
+        runs = self.runs() if grouped else [[it] for it in self.items]
+        side_run = [concurrent and self.kind == "prefill" and r[0]["case"].M <= 128 for r in runs]
+        small = [r for r, f in zip(runs, side_run) if f]
+        main = [r for r, f in zip(runs, side_run) if not f]
+        if small:
+            main = main[::-1]
+            if not hasattr(self, "_side"):
+                self._side = torch.cuda.Stream(stream.device)
+            start = torch.cuda.Event()
+            start.record(stream)
+            self._side.wait_event(start)
         n = 0
-        for run in (self.runs() if grouped else [[it] for it in self.items]):
-            if len(run) > 1:
-                binding.gemm_grouped([(it["X"], it["w"], it["Y"], False) for it in run], stream=stream)
-            else:
-                binding.gemm(run[0]["X"], run[0]["w"], out=run[0]["Y"], stream=stream)
-            n += binding.last_launch_count()
+        for st, group in ((stream, main), (getattr(self, "_side", None), small)):
+            for run in group:
+                if len(run) > 1:
+                    binding.gemm_grouped([(it["X"], it["w"], it["Y"], False) for it in run], stream=st)
+                else:
+                    binding.gemm(run[0]["X"], run[0]["w"], out=run[0]["Y"], stream=st)
+                n += binding.last_launch_count()
+        if small:
+            done = torch.cuda.Event()
+            done.record(self._side)
+            stream.wait_event(done)
         return n
 
 
@@ -389,6 +411,8 @@ def run_gpu(args, rank, world, local):
                   f"programmatic dependent launch"
                   + ("; the products of one M (a layer's four linears, independent inputs) share one grouped "
                      "launch, tm_w4a16_gemm_grouped" if launches_per_step < len(wl.items) else "")
+                  + ("; the M = 128 products on a second stream beside the others (independent products), "
+                     "joined before the step ends" if wl.kind == "prefill" else "")
                   + f"); {wl.weight_bytes} bytes of distinct packed weights per step; fp32 accumulation",
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
                      "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -814,13 +838,29 @@ def run_rtn(args, rank, world, local):
     step_bytes = sum(L["bytes"] for L in layers)
     lib = binding.load()
     stream = torch.cuda.Stream(device)
+    side = torch.cuda.Stream(device)
+
+    def quantize(L, st):
+        r = lib.tm_quantize_rtn(L["W"].data_ptr(), L["K"], L["N"], g, L["q"].data_ptr(), L["z"].data_ptr(),
+                                L["s"].data_ptr(), ctypes.c_void_p(st.cuda_stream))
+        if r != 0:
+            raise RuntimeError(f"tm_quantize_rtn failed: {r}")
+
+    # The four layers are independent: gate_up and o_proj on the launching
+    # stream, down and qkv on a second one, joined before the step ends, so
+    # that one layer's wave tail overlaps another's launch.
+    by = {L["name"]: L for L in layers}
 
     def launch_all(st):
-        for L in layers:
-            r = lib.tm_quantize_rtn(L["W"].data_ptr(), L["K"], L["N"], g, L["q"].data_ptr(), L["z"].data_ptr(),
-                                    L["s"].data_ptr(), ctypes.c_void_p(st.cuda_stream))
-            if r != 0:
-                raise RuntimeError(f"tm_quantize_rtn failed: {r}")
+        start = torch.cuda.Event()
+        start.record(st)
+        side.wait_event(start)
+        for a, b in (("gate_up", "down"), ("o_proj", "qkv")):
+            quantize(by[a], st)
+            quantize(by[b], side)
+        done = torch.cuda.Event()
+        done.record(side)
+        st.wait_event(done)
 
     with torch.cuda.stream(stream):
         launch_all(stream)
@@ -893,6 +933,8 @@ def run_rtn(args, rank, world, local):
         "config": {"workload": "rtn: qkv/o_proj/gate_up/down fp16 weights, g=128", "launches_per_step": len(layers),
                    "bytes_per_step": step_bytes,
                    "l2": "inputs larger than L2 (698 MB of fp16 weights per step)"},
+        "launch": "one CUDA graph per step: gate_up then o_proj on the launching stream, down then qkv on a "
+                  "second stream (independent layers), joined before the step ends",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": read_traffic("rtn", "llama3_8b_rtn"),
@@ -937,9 +979,21 @@ def run_silu(args, rank, world, local):
     step_bytes = sum(it["bytes"] for it in items)
     stream = torch.cuda.Stream(device)
 
+    # The four batch sizes are independent products: one stream each, joined
+    # before the step ends.
+    sides = [torch.cuda.Stream(device) for _ in items[1:]]
+
     def fused(st):
-        for it in items:
-            binding.gemm_silu_mul(it["X"], it["w"], out=it["H"], stream=st)
+        start = torch.cuda.Event()
+        start.record(st)
+        for sd in sides:
+            sd.wait_event(start)
+        for it, sd in zip(items, [st] + sides):
+            binding.gemm_silu_mul(it["X"], it["w"], out=it["H"], stream=sd)
+        for sd in sides:
+            done = torch.cuda.Event()
+            done.record(sd)
+            st.wait_event(done)
 
     def unfused(st):
         for it in items:
@@ -990,6 +1044,8 @@ def run_silu(args, rank, world, local):
                    "bytes_per_step": step_bytes, "unfused_ms_per_step": round(t_unfused / args.steps, 4),
                    "unfused": "the same GEMMs writing Y [M][N], then torch silu-mul on the interleaved halves",
                    "l2": "each GEMM has its own packed weights (235 MB per step > 129 MB L2)"},
+        "launch": "one CUDA graph per step: the four batch sizes (independent products) on four streams, "
+                  "joined before the step ends (the unfused figure: one stream)",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
                      "peak_source": peaks["source"], "kernel": "decode_kernel / tc_kernel (fused epilogue)"},
