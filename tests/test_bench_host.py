@@ -77,3 +77,29 @@ def test_kernel_hash_covers_the_listed_sources():
         for f in files:
             assert os.path.exists(os.path.join(bench.ROOT, "w4a16_quantized_gemm_gb300", "csrc", f)), (kind, f)
         assert len(bench.kernel_hash(kind)) == 16
+
+
+def _fake_workload(cases):
+    """A bench.Workload holding only the cases (no device tensors): enough for runs()."""
+    from types import SimpleNamespace
+    wl = object.__new__(bench.Workload)
+    wl.items = [{"case": SimpleNamespace(M=M, g=g, name=f"p{i}")} for i, (M, g) in enumerate(cases)]
+    return wl
+
+
+def test_step_runs_group_consecutive_products_of_one_small_m():
+    from w4a16_quantized_gemm_gb300 import binding
+    sizes = lambda wl: [len(r) for r in wl.runs()]
+    # the headline step: four linears at each of M = 1, 8, 16, 32 -> four grouped launches
+    wl = _fake_workload([(M, 128) for M in (1, 8, 16, 32) for _ in range(4)])
+    assert sizes(wl) == [4, 4, 4, 4]
+    assert all(len({it["case"].M for it in r}) == 1 for r in wl.runs())
+    # at most GROUP_MAX products a launch; a change of M or g starts a new launch
+    assert binding.GROUP_MAX == 4
+    assert sizes(_fake_workload([(1, 128)] * 6)) == [4, 2]
+    assert sizes(_fake_workload([(8, 128), (8, 64), (8, 64), (16, 64)])) == [1, 2, 1]
+    # M above 32 (the tensor-memory path) is never grouped
+    assert sizes(_fake_workload([(128, 128)] * 4 + [(33, 128)] * 2)) == [1, 1, 1, 1, 1, 1]
+    # the products keep their order
+    wl = _fake_workload([(1, 128), (1, 128), (8, 128)])
+    assert [it["case"].name for r in wl.runs() for it in r] == ["p0", "p1", "p2"]
