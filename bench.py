@@ -281,34 +281,46 @@ class Workload:
 
     def launch_all(self, stream, grouped=True, concurrent=True):
         """One step: the grouped launches of runs() (grouped=False: every
-        product launched on its own).  In the prefill workload (concurrent)
-        the M = 128 products, bound by their weight stream, run on a second
-        stream beside the tensor-bound ones (those largest first), joined
-        before the step ends; the products are independent.  Returns the
+        product launched on its own), on two streams (concurrent): the step's
+        products are independent, so one launch's start-up and tail overlap
+        another's.  Decode: the runs by M, largest with smallest -- M = 32 and
+        1 on the launching stream, 16 and 8 on the second.  Prefill: the
+        products under 60 GFLOP (every M = 128 one, qkv and o_proj at
+        M = 1024: bound by their weight stream or a badly filled wave) on the
+        second stream, the others largest first on the launching one.  The
+        second stream joins the first before the step ends.  Returns the
         number of kernel launches."""
         import torch
 
         from w4a16_quantized_gemm_gb300 import binding
         runs = self.runs() if grouped else [[it] for it in self.items]
-        side_run = [concurrent and self.kind == "prefill" and r[0]["case"].M <= 128 for r in runs]
-        small = [r for r, f in zip(runs, side_run) if f]
-        main = [r for r, f in zip(runs, side_run) if not f]
-        if small:
-            main = main[::-1]
+        main, side = runs, []
+        if concurrent and self.kind == "decode" and len(runs) > 1:
+            order = sorted(range(len(runs)), key=lambda i: -runs[i][0]["case"].M)
+            lanes = [[], []]
+            for j in range((len(order) + 1) // 2):  # the j-th largest with the j-th smallest
+                ids = [order[j]] + ([order[-1 - j]] if len(order) - 1 - j != j else [])
+                lanes[j % 2].extend(runs[i] for i in ids)
+            main, side = lanes
+        elif concurrent and self.kind == "prefill":
+            small = [flops(r[0]["case"].M, r[0]["case"].K, r[0]["case"].N) < 60e9 for r in runs]
+            side = [r for r, f in zip(runs, small) if f]
+            main = [r for r, f in zip(runs, small) if not f][::-1]
+        if side:
             if not hasattr(self, "_side"):
                 self._side = torch.cuda.Stream(stream.device)
             start = torch.cuda.Event()
             start.record(stream)
             self._side.wait_event(start)
         n = 0
-        for st, group in ((stream, main), (getattr(self, "_side", None), small)):
+        for st, group in ((stream, main), (getattr(self, "_side", None), side)):
             for run in group:
                 if len(run) > 1:
                     binding.gemm_grouped([(it["X"], it["w"], it["Y"], False) for it in run], stream=st)
                 else:
                     binding.gemm(run[0]["X"], run[0]["w"], out=run[0]["Y"], stream=st)
                 n += binding.last_launch_count()
-        if small:
+        if side:
             done = torch.cuda.Event()
             done.record(self._side)
             stream.wait_event(done)
@@ -411,8 +423,10 @@ def run_gpu(args, rank, world, local):
                   f"programmatic dependent launch"
                   + ("; the products of one M (a layer's four linears, independent inputs) share one grouped "
                      "launch, tm_w4a16_gemm_grouped" if launches_per_step < len(wl.items) else "")
-                  + ("; the M = 128 products on a second stream beside the others (independent products), "
-                     "joined before the step ends" if wl.kind == "prefill" else "")
+                  + ("; the launches on two streams (independent products): M = 32 and 1 on the launching "
+                     "stream, 16 and 8 on a second, joined before the step ends" if wl.kind == "decode" else "")
+                  + ("; the products under 60 GFLOP (M = 128, qkv and o_proj at M = 1024) on a second stream "
+                     "beside the others, joined before the step ends" if wl.kind == "prefill" else "")
                   + f"); {wl.weight_bytes} bytes of distinct packed weights per step; fp32 accumulation",
         "roofline": {"bound": spec["bound"], "achieved": round(achieved, 2), "peak": peak,
                      "unit": unit_kernel, "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -620,10 +634,12 @@ def config_detail(wl, stream, peaks, args, min_bytes=300e6, reps=5):
                                          f"{how}", "grouped": grouped,
                     "us": round(t * 1e6, 2), "GB/s": round(nb / t / 1e9, 1),
                     "roofline": roofline_entry(nb, 0, t, peaks)})
-    ms = _time_graph(lambda st: dwl.launch_all(st, grouped=False), stream, 20)
-    out.append({"config": 1, "step": "llama3-8b decode step, the 16 GEMMs launched one by one (16 launches)",
-                "us": round(ms * 1e3, 2), "GB/s": round(dwl.step_bytes / (ms * 1e-3) / 1e9, 1),
-                "roofline": roofline_entry(dwl.step_bytes, dwl.step_flops, ms * 1e-3, peaks)})
+    for grouped, what in ((False, "the 16 GEMMs launched one by one on one stream (16 launches)"),
+                          (True, "one grouped launch per M on one stream (4 launches)")):
+        ms = _time_graph(lambda st: dwl.launch_all(st, grouped=grouped, concurrent=False), stream, 20)
+        out.append({"config": 1, "step": f"llama3-8b decode step, {what}",
+                    "us": round(ms * 1e3, 2), "GB/s": round(dwl.step_bytes / (ms * 1e-3) / 1e9, 1),
+                    "roofline": roofline_entry(dwl.step_bytes, dwl.step_flops, ms * 1e-3, peaks)})
     out.append(_decode_step_concurrent(dwl, stream, peaks))
     out.append(_prefill_step(device, stream, peaks, max(5, min(args.steps, 50))))
     return out
