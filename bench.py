@@ -1254,26 +1254,34 @@ def run_w8a8(args, rank, world, local, prefill=False):
     # quantiser (HBM-bound) overlaps the GEMMs before it (tensor-bound in
     # prefill); the second stream joins the first before the step ends.
     side = torch.cuda.Stream(device)
+    lane2 = torch.cuda.Stream(device)
+    # The GEMMs on two lanes as in the W4A16 steps: decode M = 16 and 8, or
+    # the prefill products under 60 GFLOP, on a second GEMM stream.
+    second = [(it["M"] in (8, 16)) if not prefill else (it["flops"] < 60e9) for it in items]
+    w8_streams = args.w8_streams
 
     def launch_all(st):
         start = torch.cuda.Event()
         start.record(st)
         side.wait_event(start)
-        for it in items:
+        lane2.wait_event(start)
+        for it, two in zip(items, second):
+            gst = lane2 if (two and w8_streams > 2) else st
             if codes == "int8":
                 binding.w8a8_quantize_act(it["X"], out=(it["xq"], it["sx"]), stream=side)
             else:
                 binding.w8a8_quantize_act_f16(it["X"], out=(it["xq"], it["sx"]), stream=side)
             ready = torch.cuda.Event()
             ready.record(side)
-            st.wait_event(ready)
+            gst.wait_event(ready)
             if codes == "int8":
-                binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=st)
+                binding.w8a8_gemm(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=gst)
             else:
-                binding.w8a8_gemm_f16(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=st)
-        done = torch.cuda.Event()
-        done.record(side)
-        st.wait_event(done)
+                binding.w8a8_gemm_f16(it["xq"], it["sx"], it["w"], out=it["Y"], tile_m=args.w8_tile_m, stream=gst)
+        for sd in (side, lane2):
+            done = torch.cuda.Event()
+            done.record(sd)
+            st.wait_event(done)
 
     with torch.cuda.stream(stream):
         launch_all(stream)
@@ -1343,7 +1351,9 @@ def run_w8a8(args, rank, world, local, prefill=False):
                    "activation_codes": codes, "tile_m": args.w8_tile_m or "auto",
                    "launches_per_step": 2 * len(items), "bytes_per_step": step_bytes, "flops_per_step": step_flops,
                    "streams": "the activation quantisers on a second stream, each GEMM waiting for its own "
-                              "quantiser (the products are independent)",
+                              "quantiser (the products are independent)"
+                              + ("; the GEMMs of M = 16 and 8 (decode) or under 60 GFLOP (prefill) on a third"
+                                 if args.w8_streams > 2 else ""),
                    "l2": f"each GEMM has its own packed weights ({weight_bytes / 1e6:.0f} MB per step > 129 MB L2)"},
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4),
@@ -1419,6 +1429,8 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--w8-streams", type=int, default=3, choices=(2, 3),
+                   help="W8A8 workloads: 2 = quantisers on a second stream; 3 = also the smaller GEMMs on a third")
     p.add_argument("--workload", choices=sorted(WORKLOADS) + ["rtn", "silu", "kv", "w8a8", "w8a8_prefill"],
                    default="decode")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
