@@ -294,18 +294,7 @@ class Workload:
 
         from w4a16_quantized_gemm_gb300 import binding
         runs = self.runs() if grouped else [[it] for it in self.items]
-        main, side = runs, []
-        if concurrent and self.kind == "decode" and len(runs) > 1:
-            order = sorted(range(len(runs)), key=lambda i: -runs[i][0]["case"].M)
-            lanes = [[], []]
-            for j in range((len(order) + 1) // 2):  # the j-th largest with the j-th smallest
-                ids = [order[j]] + ([order[-1 - j]] if len(order) - 1 - j != j else [])
-                lanes[j % 2].extend(runs[i] for i in ids)
-            main, side = lanes
-        elif concurrent and self.kind == "prefill":
-            small = [flops(r[0]["case"].M, r[0]["case"].K, r[0]["case"].N) < 60e9 for r in runs]
-            side = [r for r, f in zip(runs, small) if f]
-            main = [r for r, f in zip(runs, small) if not f][::-1]
+        main, side = split_lanes(runs, self.kind) if concurrent else (runs, [])
         if side:
             if not hasattr(self, "_side"):
                 self._side = torch.cuda.Stream(stream.device)
@@ -325,6 +314,25 @@ class Workload:
             done.record(self._side)
             stream.wait_event(done)
         return n
+
+
+def split_lanes(runs, kind):
+    """The two streams of a step's launches (launching stream, second stream).
+    Decode: the runs by M, the j-th largest with the j-th smallest on lane j % 2
+    (M = 32 and 1 on the launching stream, 16 and 8 on the second).  Prefill:
+    the products under 60 GFLOP on the second stream, the others largest
+    first on the launching one.  Anything else: one stream."""
+    if kind == "decode" and len(runs) > 1:
+        order = sorted(range(len(runs)), key=lambda i: -runs[i][0]["case"].M)
+        lanes = [[], []]
+        for j in range((len(order) + 1) // 2):
+            ids = [order[j]] + ([order[-1 - j]] if len(order) - 1 - j != j else [])
+            lanes[j % 2].extend(runs[i] for i in ids)
+        return lanes[0], lanes[1]
+    if kind == "prefill":
+        small = [flops(r[0]["case"].M, r[0]["case"].K, r[0]["case"].N) < 60e9 for r in runs]
+        return [r for r, f in zip(runs, small) if not f][::-1], [r for r, f in zip(runs, small) if f]
+    return runs, []
 
 
 def run_gpu(args, rank, world, local):

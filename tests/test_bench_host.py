@@ -103,3 +103,27 @@ def test_step_runs_group_consecutive_products_of_one_small_m():
     # the products keep their order
     wl = _fake_workload([(1, 128), (1, 128), (8, 128)])
     assert [it["case"].name for r in wl.runs() for it in r] == ["p0", "p1", "p2"]
+
+
+def test_step_lanes_pair_large_with_small_m_and_move_small_prefill_products():
+    from types import SimpleNamespace
+    run = lambda M, K=4096, N=4096: [{"case": SimpleNamespace(M=M, K=K, N=N)}]
+    Ms = lambda lane: [r[0]["case"].M for r in lane]
+    # decode: M = 32 with 1 on the launching stream, 16 with 8 on the second
+    main, side = bench.split_lanes([run(M) for M in (1, 8, 16, 32)], "decode")
+    assert (Ms(main), Ms(side)) == ([32, 1], [16, 8])
+    main, side = bench.split_lanes([run(M) for M in (1, 8, 16)], "decode")
+    assert (Ms(main), Ms(side)) == ([16, 1], [8])
+    assert bench.split_lanes([run(4)], "decode") == ([run(4)], [])
+    # prefill: the products under 60 GFLOP (2MKN) on the second stream, the rest largest first
+    shapes = {"qkv": (4096, 6144), "o_proj": (4096, 4096), "gate_up": (4096, 28672), "down": (14336, 4096)}
+    runs = [run(M, K, N) for M in (128, 1024, 4096) for K, N in shapes.values()]
+    main, side = bench.split_lanes(runs, "prefill")
+    assert Ms(side) == [128, 128, 128, 128, 1024, 1024]
+    assert [(r[0]["case"].K, r[0]["case"].N) for r in side[4:]] == [shapes["qkv"], shapes["o_proj"]]
+    assert Ms(main) == [4096, 4096, 4096, 4096, 1024, 1024]
+    assert all(bench.flops(r[0]["case"].M, r[0]["case"].K, r[0]["case"].N) >= 60e9 for r in main)
+    # every run once
+    assert len(main) + len(side) == len(runs)
+    # other workloads: one stream
+    assert bench.split_lanes(runs, "stress") == (runs, [])
