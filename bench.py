@@ -441,9 +441,10 @@ def run_gpu(args, rank, world, local):
                      "peak_source": peaks["source"],
                      "kernel": "decode_kernel" if spec["bound"] == "hbm" else "tc_kernel",
                      "basis": "algorithmic units of the step's launches / mean step time of the timed "
-                              "region (CUDA events around each graph replay); consecutive launches overlap "
-                              "under programmatic dependent launch, so the step time is their combined "
-                              "duration and the average launch duration is step time / launches",
+                              "region (CUDA events around each graph replay, the step's streams joined "
+                              "before its closing event); the launches overlap (programmatic dependent "
+                              "launch, and two streams where the step uses them), so the step time stands "
+                              "for their combined duration",
                      "launches_per_step": launches_per_step},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
